@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the benchmark and the oracle's tests.
+
+This module only draws random numbers and names shapes.  It holds none of the attention
+arithmetic, so importing it from both sides keeps the oracle and the CUDA path independent.
+
+Recipe (one per workload):
+  * ``torch.Generator('cpu').manual_seed(seed)``; Q, K, V, dO drawn in that order with
+    ``randn`` in fp32 of shape [B, H, N, d], then cast to the workload dtype.
+  * The long-context workload multiplies Q and K by 2 before the cast (a power of two, so the
+    cast of the doubled value equals the double of the cast value).
+  * The block-sparse workload's 128x128 block mask: generator seeded with ``seed + 1000``;
+    off-diagonal blocks kept iid with probability 0.25, every diagonal block kept.
+
+The five workloads follow the shapes of the FlashAttention-2 reading notes' kernel benchmark
+(seq 512-16k, hidden 2048, heads of 64/128) and the GPT-style 8k training shape the notes quote.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+BLOCK = 128  # block-mask granularity (rows and columns of the score matrix per mask entry)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str            # "fp16" or "bf16"
+    causal: bool
+    seed: int
+    qk_mult: float = 1.0  # multiplier applied to Q and K before the cast
+    sparse_p: Optional[float] = None  # Bernoulli keep-probability of off-diagonal mask blocks
+    backward: bool = True
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float16 if self.dtype == "fp16" else torch.bfloat16
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def tiles(self) -> int:
+        return (self.N + BLOCK - 1) // BLOCK
+
+    def describe(self) -> str:
+        kind = "block-sparse" if self.sparse_p is not None else ("causal" if self.causal else "dense")
+        passes = "fwd+bwd" if self.backward else "fwd"
+        return (f"{self.name}: {passes} {kind} B={self.B} H={self.H} N={self.N} d={self.d} "
+                f"{self.dtype}")
+
+
+WORKLOADS: Dict[str, Workload] = {
+    # single-tile forward case, small enough for the fp64 oracle in well under a second
+    "tiny_fwd_fp16": Workload("tiny_fwd_fp16", 1, 1, 128, 64, "fp16", False, 1, backward=False),
+    # non-causal head-64 forward+backward
+    "dense_d64_n1k": Workload("dense_d64_n1k", 4, 16, 1024, 64, "bf16", False, 2),
+    # causal head-128 forward+backward
+    "causal_d128_n4k": Workload("causal_d128_n4k", 2, 16, 4096, 128, "bf16", True, 3),
+    # GPT-style long-context training shape, scores widened by doubling Q and K
+    "gpt_causal_d128_n8k": Workload("gpt_causal_d128_n8k", 1, 32, 8192, 128, "bf16", True, 4,
+                                    qk_mult=2.0),
+    # block-sparse head-64 forward+backward at 16k tokens, density about 0.256
+    "blocksparse_d64_n16k": Workload("blocksparse_d64_n16k", 1, 8, 16384, 64, "bf16", False, 5,
+                                     sparse_p=0.25),
+}
+
+ORDER = ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k", "gpt_causal_d128_n8k",
+         "blocksparse_d64_n16k"]
+
+
+def make_inputs(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
+                qk_mult: float = 1.0, with_dout: bool = True) -> Dict[str, torch.Tensor]:
+    """Draw Q, K, V (and dO) on the CPU from one seeded generator, in that order."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    out = {}
+    if qk_mult != 1.0:
+        q = q * qk_mult
+        k = k * qk_mult
+    out["q"] = q.to(dtype)
+    out["k"] = k.to(dtype)
+    out["v"] = v.to(dtype)
+    if with_dout:
+        out["do"] = torch.randn(shape, generator=g, dtype=torch.float32).to(dtype)
+    return out
+
+
+def make_block_mask(tiles: int, seed: int, p: float, keep_diagonal: bool = True) -> torch.Tensor:
+    """uint8 [tiles, tiles] row-major: 1 keeps a 128x128 score block, 0 skips it."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    m = (torch.rand((tiles, tiles), generator=g) < p).to(torch.uint8)
+    if keep_diagonal:
+        idx = torch.arange(tiles)
+        m[idx, idx] = 1
+    return m.contiguous()
+
+
+def workload_inputs(w: Workload) -> Dict[str, torch.Tensor]:
+    out = make_inputs(w.B, w.H, w.N, w.d, w.torch_dtype, w.seed, w.qk_mult, with_dout=True)
+    if w.sparse_p is not None:
+        out["block_mask"] = make_block_mask(w.tiles, w.seed + 1000, w.sparse_p)
+    return out

@@ -1,0 +1,178 @@
+"""fp64 CPU oracle for exact attention.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares nothing with the CUDA library; the two meet
+only through the seeded inputs of ``exact_attention_staged_gb300.workloads``.
+
+``attn_oracle.c`` holds the definition (see its header for the citations); ``recurrence.py``
+holds the tiled online-softmax recurrences the pages derive, used to pin the definition.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` (worked example,
+closed forms, invariants, finite differences, library special cases).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_SO = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_lp = ctypes.POINTER(ctypes.c_long)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (plain -O2, IEEE arithmetic, OpenMP)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC,
+                               "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_SO)
+            lib.oracle_attention.argtypes = [ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                             ctypes.c_long, _dp, _dp, _dp, _dp, ctypes.c_double,
+                                             ctypes.c_int, _u8p, ctypes.c_int, _dp, _dp, _dp, _dp,
+                                             _dp, _dp]
+            lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_forward_rows.argtypes = [ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                _dp, _dp, _dp,
+                                                ctypes.c_double, ctypes.c_int, _u8p, ctypes.c_int,
+                                                ctypes.c_long, _lp, _dp, _dp]
+            lib.oracle_forward_rows.restype = ctypes.c_int
+            for name in ("oracle_scores", "oracle_probabilities"):
+                fn = getattr(lib, name)
+                fn.argtypes = [ctypes.c_long, ctypes.c_long, ctypes.c_long, _dp, _dp,
+                               ctypes.c_double,
+                               ctypes.c_int, _u8p, ctypes.c_int, _dp]
+                fn.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast of fp16/bf16/fp32 values (numpy arrays or CPU torch tensors) to fp64."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _mask_arg(block_mask, N: int, block: int):
+    """N is max(Nq, Nk): the mask is square with ceil(N / block) tiles per side."""
+    if block_mask is None:
+        return None, None
+    m = block_mask
+    if hasattr(m, "detach"):
+        m = m.detach().cpu().numpy()
+    m = np.ascontiguousarray(np.asarray(m, dtype=np.uint8))
+    tiles = (N + block - 1) // block
+    if m.shape != (tiles, tiles):
+        raise ValueError(f"block mask must be [{tiles},{tiles}], got {m.shape}")
+    return m, m.ctypes.data_as(_u8p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def attention(q, k, v, scale: float, causal: bool = False, block_mask=None, block: int = 128,
+              dout=None) -> dict:
+    """Forward (and backward when ``dout`` is given): q [..., Nq, d], k and v [..., Nk, d].
+
+    Returns fp64 arrays: o, lse and, with ``dout``, dq, dk, dv and delta (D_i = <P_i, dP_i>).
+    """
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    if qa.ndim < 2 or ka.shape != va.shape or qa.shape[:-2] != ka.shape[:-2] \
+            or qa.shape[-1] != ka.shape[-1]:
+        raise ValueError("q must be [..., Nq, d] and k, v [..., Nk, d]")
+    *lead, Nq, d = qa.shape
+    Nk = ka.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    mk, mptr = _mask_arg(block_mask, max(Nq, Nk), block)
+    o = np.empty_like(qa)
+    lse = np.empty(tuple(lead) + (Nq,), dtype=np.float64)
+    res = {"o": o, "lse": lse}
+    null = ctypes.cast(None, _dp)
+    if dout is not None:
+        da = _f64(dout)
+        if da.shape != qa.shape:
+            raise ValueError("dout must match q")
+        dq, dk, dv = np.empty_like(qa), np.empty_like(ka), np.empty_like(ka)
+        delta = np.empty_like(lse)
+        rc = _load().oracle_attention(BH, Nq, Nk, d, _ptr(qa), _ptr(ka), _ptr(va), _ptr(da),
+                                      float(scale), int(bool(causal)), mptr, block, _ptr(o),
+                                      _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta))
+        res.update(dq=dq, dk=dk, dv=dv, delta=delta)
+    else:
+        rc = _load().oracle_attention(BH, Nq, Nk, d, _ptr(qa), _ptr(ka), _ptr(va), null,
+                                      float(scale),
+                                      int(bool(causal)), mptr, block, _ptr(o), _ptr(lse), null,
+                                      null, null, null)
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention failed ({rc})")
+    del mk
+    return res
+
+
+def forward_rows(q, k, v, scale: float, rows, causal: bool = False, block_mask=None,
+                 block: int = 128):
+    """O and LSE for the given query rows of ONE head (q: [Nq, d]; k, v: [Nk, d])."""
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    Nq, d = qa.shape
+    Nk = ka.shape[0]
+    mk, mptr = _mask_arg(block_mask, max(Nq, Nk), block)
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    o = np.empty((len(r), d), dtype=np.float64)
+    lse = np.empty((len(r),), dtype=np.float64)
+    rc = _load().oracle_forward_rows(Nq, Nk, d, _ptr(qa), _ptr(ka), _ptr(va), float(scale),
+                                     int(bool(causal)), mptr, block, len(r),
+                                     r.ctypes.data_as(_lp), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise RuntimeError(f"oracle_forward_rows failed ({rc})")
+    del mk
+    return o, lse
+
+
+def _square(name, q, k, scale, causal, block_mask, block):
+    qa, ka = _f64(q), _f64(k)
+    Nq, d = qa.shape
+    Nk = ka.shape[0]
+    mk, mptr = _mask_arg(block_mask, max(Nq, Nk), block)
+    out = np.empty((Nq, Nk), dtype=np.float64)
+    rc = getattr(_load(), name)(Nq, Nk, d, _ptr(qa), _ptr(ka), float(scale), int(bool(causal)), mptr,
+                                block, _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"{name} failed ({rc})")
+    del mk
+    return out
+
+
+def scores(q, k, scale: float, causal: bool = False, block_mask=None, block: int = 128):
+    """S = scale * Q K^T of ONE head with -inf at masked entries."""
+    return _square("oracle_scores", q, k, scale, causal, block_mask, block)
+
+
+def probabilities(q, k, scale: float, causal: bool = False, block_mask=None, block: int = 128):
+    """P = softmax(S) of ONE head (three-pass safe softmax)."""
+    return _square("oracle_probabilities", q, k, scale, causal, block_mask, block)

@@ -1,0 +1,313 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Every check compares the oracle with something other than itself: the worked example printed
+on the wmrh.cn page, closed forms, library routines (scipy, torch autograd), the pages' own
+tiled recurrences, brute force and finite differences.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import recurrence
+from exact_attention_staged_gb300.workloads import make_block_mask, make_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- worked example (wmrh.cn page)
+
+def _golden():
+    with open(os.path.join(GOLDEN, "online_softmax_worked_example.json")) as f:
+        return json.load(f)
+
+
+def test_worked_example_recurrence_matches_printed_m_and_terms():
+    g = _golden()
+    steps = recurrence.online_softmax_tiles(g["tiles"])
+    ms = [s[0] for s in steps]
+    ls = [s[1] for s in steps]
+    assert ms == g["printed_row_m"]                       # 2.0, 3.0, 3.0 exactly
+    assert round(ls[0], 2) == g["printed_row_l"][0]       # 1.37 as printed
+    prev = None
+    for i, term in enumerate(g["printed_terms"]):
+        # evaluate the page's own written term on the exact previous l
+        want = sum(math.exp(e) for e in term["exponents"])
+        if term["prev_factor_exponent"] is not None:
+            want += prev * math.exp(term["prev_factor_exponent"])
+        assert ls[i] == pytest.approx(want, rel=1e-14), term["text"]
+        prev = ls[i]
+    # the page's printed 1.88 and 3.03 are arithmetic slips (reading recorded in the fixture)
+    assert abs(ls[1] - g["printed_row_l"][1]) > 0.2
+    assert abs(ls[2] - g["printed_row_l"][2]) > 0.5
+
+
+def test_worked_example_final_stats_equal_three_pass_oracle():
+    g = _golden()
+    x = np.concatenate([np.asarray(t) for t in g["tiles"]])
+    n = len(x)
+    # one query row with q = 1 against keys k_j = x_j (d = 1, scale 1) makes S_0j = x_j
+    q = np.zeros((n, 1)); q[0, 0] = 1.0
+    k = x.reshape(n, 1).copy()
+    v = rand((n, 1), 0)
+    res = oracle.attention(q, k, v, scale=1.0)
+    steps = recurrence.online_softmax_tiles(g["tiles"])
+    m, l = steps[-1]
+    assert res["lse"][0] == pytest.approx(m + math.log(l), abs=1e-13)
+    assert res["lse"][0] == pytest.approx(scipy.special.logsumexp(x), abs=1e-13)
+    # scalar (element-by-element) recurrence of the "Flash Attention v1" page agrees too
+    ms, ds = recurrence.online_softmax_scalar(x)
+    assert ms == 3.0 and ds == pytest.approx(l, rel=1e-14)
+    # merging two halves' statistics gives the same (FlashAttention paper-detail page)
+    m1, l1 = recurrence.online_softmax_scalar(x[:3])
+    m2, l2 = recurrence.online_softmax_scalar(x[3:])
+    mm, lm = recurrence.merge_stats(m1, l1, m2, l2)
+    assert mm == 3.0 and lm == pytest.approx(l, rel=1e-14)
+
+
+# ---------------------------------------------------------------- forward: library and closed forms
+
+@pytest.mark.parametrize("N,d", [(1, 4), (7, 3), (33, 16), (64, 8)])
+def test_forward_matches_scipy_softmax(N, d):
+    q, k, v = rand((N, d), 1), rand((N, d), 2), rand((N, d), 3)
+    scale = 0.37
+    res = oracle.attention(q, k, v, scale)
+    S = scale * (q @ k.T)
+    np.testing.assert_allclose(res["lse"], scipy.special.logsumexp(S, axis=1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(res["o"], scipy.special.softmax(S, axis=1) @ v, rtol=0, atol=1e-12)
+
+
+def test_two_keys_reduce_to_a_sigmoid():
+    # softmax over two scores is the logistic function of their difference
+    rng = np.random.default_rng(5)
+    d = 6
+    q, k, v = rng.standard_normal((2, d)), rng.standard_normal((2, d)), rng.standard_normal((2, d))
+    scale = 0.8
+    res = oracle.attention(q, k, v, scale)
+    for i in range(2):
+        z = scale * float(q[i] @ (k[0] - k[1]))
+        sig = 1.0 / (1.0 + math.exp(-z))
+        np.testing.assert_allclose(res["o"][i], v[1] + (v[0] - v[1]) * sig, atol=1e-14)
+        s0, s1 = scale * float(q[i] @ k[0]), scale * float(q[i] @ k[1])
+        assert res["lse"][i] == pytest.approx(max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))),
+                                              abs=1e-14)
+
+
+def test_equal_value_rows_give_that_row():
+    N, d = 40, 8
+    q, k = rand((N, d), 7, 3.0), rand((N, d), 8, 3.0)
+    row = rand((d,), 9)
+    v = np.tile(row, (N, 1))
+    for causal in (False, True):
+        res = oracle.attention(q, k, v, 0.5, causal=causal)
+        np.testing.assert_allclose(res["o"], np.tile(row, (N, 1)), atol=1e-12)
+
+
+def test_uniform_scores_average_the_values():
+    N, d = 21, 5
+    q = np.zeros((N, d))
+    k, v = rand((N, d), 10), rand((N, d), 11)
+    res = oracle.attention(q, k, v, 1.0)
+    np.testing.assert_allclose(res["o"], np.tile(v.mean(axis=0), (N, 1)), atol=1e-13)
+    np.testing.assert_allclose(res["lse"], np.full(N, math.log(N)), atol=1e-13)
+    res = oracle.attention(q, k, v, 1.0, causal=True)
+    want = np.cumsum(v, axis=0) / np.arange(1, N + 1)[:, None]
+    np.testing.assert_allclose(res["o"], want, atol=1e-13)
+    np.testing.assert_allclose(res["lse"], np.log(np.arange(1, N + 1)), atol=1e-13)
+
+
+def test_rows_of_p_sum_to_one_and_scores_never_exceed_lse():
+    N, d = 300, 16
+    q, k, v = rand((N, d), 12, 2.0), rand((N, d), 13, 2.0), rand((N, d), 14)
+    mask = make_block_mask(3, 99, 0.5).numpy()
+    for causal, m in ((False, None), (True, None), (False, mask), (True, mask)):
+        P = oracle.probabilities(q, k, 0.25, causal=causal, block_mask=m)
+        S = oracle.scores(q, k, 0.25, causal=causal, block_mask=m)
+        lse = oracle.attention(q, k, v, 0.25, causal=causal, block_mask=m)["lse"]
+        assert np.all(np.abs(P.sum(axis=1) - 1.0) <= 1e-12)
+        assert np.all(P >= 0) and np.all(P <= 1)
+        assert np.all(S - lse[:, None] <= 0)
+
+
+def test_causal_matches_brute_force_row_loop():
+    N, d = 19, 4
+    q, k, v = rand((N, d), 15), rand((N, d), 16), rand((N, d), 17)
+    res = oracle.attention(q, k, v, 0.9, causal=True)
+    for i in range(N):
+        s = [0.9 * float(q[i] @ k[j]) for j in range(i + 1)]
+        mx = max(s)
+        w = [math.exp(x - mx) for x in s]
+        tot = sum(w)
+        o = sum(w[j] / tot * v[j] for j in range(i + 1))
+        np.testing.assert_allclose(res["o"][i], o, atol=1e-13)
+        assert res["lse"][i] == pytest.approx(mx + math.log(tot), abs=1e-13)
+
+
+def test_block_mask_all_ones_equals_dense_and_masking_drops_blocks():
+    N, d, blk = 70, 4, 16
+    q, k, v = rand((N, d), 18), rand((N, d), 19), rand((N, d), 20)
+    tiles = (N + blk - 1) // blk
+    ones = np.ones((tiles, tiles), dtype=np.uint8)
+    a = oracle.attention(q, k, v, 0.5, block_mask=ones, block=blk)
+    b = oracle.attention(q, k, v, 0.5)
+    assert np.array_equal(a["o"], b["o"]) and np.array_equal(a["lse"], b["lse"])
+    m = make_block_mask(tiles, 3, 0.4).numpy()
+    c = oracle.attention(q, k, v, 0.5, block_mask=m, block=blk)
+    for i in range(N):
+        keep = [j for j in range(N) if m[i // blk, j // blk]]
+        S = 0.5 * (q[i] @ k[keep].T)
+        np.testing.assert_allclose(c["o"][i], scipy.special.softmax(S) @ v[keep], atol=1e-13)
+
+
+def test_fully_masked_rows_are_zero():
+    N, d, blk = 48, 4, 16
+    q, k, v, do = (rand((N, d), s) for s in (21, 22, 23, 24))
+    m = np.ones((3, 3), dtype=np.uint8)
+    m[1, :] = 0
+    res = oracle.attention(q, k, v, 0.5, block_mask=m, block=blk, dout=do)
+    rows = slice(16, 32)
+    assert np.all(res["o"][rows] == 0) and np.all(np.isneginf(res["lse"][rows]))
+    assert np.all(res["dq"][rows] == 0)
+    assert np.all(np.isfinite(res["dk"])) and np.all(np.isfinite(res["dv"]))
+
+
+def test_forward_rows_match_full_forward():
+    N, d = 200, 16
+    q, k, v = rand((N, d), 25), rand((N, d), 26), rand((N, d), 27)
+    mask = make_block_mask(2, 4, 0.5).numpy()
+    full = oracle.attention(q, k, v, 0.3, causal=True, block_mask=mask)
+    rows = [0, 5, 127, 128, 199]
+    o, lse = oracle.forward_rows(q, k, v, 0.3, rows, causal=True, block_mask=mask)
+    np.testing.assert_allclose(o, full["o"][rows], atol=1e-14)
+    np.testing.assert_allclose(lse, full["lse"][rows], atol=1e-14)
+
+
+# ---------------------------------------------------------------- Theorem 1 and the recurrences
+
+@pytest.mark.parametrize("bc", [1, 2, 3, 5, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_theorem1_invariant_at_every_block_boundary(bc, causal):
+    N, d, scale = 48, 8, 0.6
+    q, k, v = rand((N, d), 30, 2.0), rand((N, d), 31, 2.0), rand((N, d), 32)
+    S = oracle.scores(q, k, scale, causal=causal)
+    steps, (O, L) = recurrence.fa2_forward_steps(S, v, bc)
+    for j, (m, l, Ot) in enumerate(steps):
+        n = min((j + 1) * bc, N)
+        pref = oracle.attention(q, k[:n], v[:n], scale) if not causal else None
+        if causal:
+            # prefix of a causal row: keys 0..min(i, n-1); rows with none are still empty
+            for i in range(N):
+                kk = min(i + 1, n)
+                r = oracle.attention(q[i:i + 1], k[:kk], v[:kk], scale)
+                assert m[i] + math.log(l[i]) == pytest.approx(r["lse"][0], abs=1e-12)
+                np.testing.assert_allclose(Ot[i] / l[i], r["o"][0], atol=1e-12)
+        else:
+            np.testing.assert_allclose(m + np.log(l), pref["lse"], atol=1e-12)
+            np.testing.assert_allclose(Ot / l[:, None], pref["o"], atol=1e-12)
+            # m is the running row max of the prefix
+            np.testing.assert_array_equal(m, S[:, :n].max(axis=1))
+    full = oracle.attention(q, k, v, scale, causal=causal)
+    np.testing.assert_allclose(O, full["o"], atol=1e-12)
+    np.testing.assert_allclose(L, full["lse"], atol=1e-12)
+
+
+def test_fa1_normalised_update_gives_same_output():
+    N, d = 37, 6
+    q, k, v = rand((N, d), 33), rand((N, d), 34), rand((N, d), 35)
+    S = oracle.scores(q, k, 1.1)
+    for bc in (1, 4, 10):
+        np.testing.assert_allclose(recurrence.fa1_forward(S, v, bc),
+                                   oracle.attention(q, k, v, 1.1)["o"], atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, do, scale, causal, mask, blk):
+    return float(np.sum(oracle.attention(q, k, v, scale, causal, mask, blk)["o"] * do))
+
+
+@pytest.mark.parametrize("N,d,causal,masked", [(5, 4, False, False), (16, 8, True, False),
+                                               (12, 4, False, True), (16, 4, True, True)])
+def test_gradients_match_central_differences(N, d, causal, masked):
+    blk = 4
+    q, k, v, do = rand((N, d), 40), rand((N, d), 41), rand((N, d), 42), rand((N, d), 43)
+    mask = make_block_mask((N + blk - 1) // blk, 7, 0.5).numpy() if masked else None
+    scale = 0.7
+    res = oracle.attention(q, k, v, scale, causal, mask, blk, dout=do)
+    h = 1e-6
+    for name, x, g in (("q", q, res["dq"]), ("k", k, res["dk"]), ("v", v, res["dv"])):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            lp = _loss(args["q"], args["k"], args["v"], do, scale, causal, mask, blk)
+            args[name] = xm
+            lm = _loss(args["q"], args["k"], args["v"], do, scale, causal, mask, blk)
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-300)
+        assert err <= 1e-6, (name, err)
+
+
+def test_gradients_match_torch_autograd_fp64():
+    N, d, blk = 96, 16, 32
+    q, k, v, do = (rand((2, N, d), s) for s in (50, 51, 52, 53))
+    mask = make_block_mask(3, 11, 0.5).numpy()
+    scale = 0.25
+    res = oracle.attention(q, k, v, scale, True, mask, blk, dout=do)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    S = scale * tq @ tk.transpose(-1, -2)
+    i = torch.arange(N)
+    keep = (i[None, :] <= i[:, None]) & torch.tensor(mask, dtype=torch.bool)[i // blk][:, i // blk]
+    S = S.masked_fill(~keep, float("-inf"))
+    O = torch.softmax(S, dim=-1) @ tv
+    O.backward(torch.tensor(do))
+    np.testing.assert_allclose(res["o"], O.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(res["lse"], torch.logsumexp(S, -1).detach().numpy(), atol=1e-12)
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(res[name], t.grad.numpy(), atol=1e-11)
+
+
+def test_delta_equals_rowsum_of_do_times_o():
+    N, d = 50, 8
+    q, k, v, do = (rand((N, d), s) for s in (60, 61, 62, 63))
+    for causal in (False, True):
+        res = oracle.attention(q, k, v, 0.4, causal, dout=do)
+        np.testing.assert_allclose(res["delta"], np.sum(do * res["o"], axis=1), atol=1e-12)
+
+
+def test_single_key_special_cases():
+    d = 6
+    q, k, v, do = (rand((1, d), s) for s in (70, 71, 72, 73))
+    res = oracle.attention(q, k, v, 0.5, dout=do)
+    np.testing.assert_allclose(res["o"], v, atol=0)
+    assert res["lse"][0] == pytest.approx(0.5 * float(q[0] @ k[0]), abs=1e-15)
+    assert np.all(res["dq"] == 0) and np.all(res["dk"] == 0)
+    np.testing.assert_allclose(res["dv"], do, atol=0)
+    # causal row 0 sees only key 0: same closed forms for that row
+    N = 9
+    q, k, v, do = (rand((N, d), s) for s in (74, 75, 76, 77))
+    res = oracle.attention(q, k, v, 0.5, causal=True, dout=do)
+    np.testing.assert_allclose(res["o"][0], v[0], atol=0)
+    assert np.all(res["dq"][0] == 0)
+
+
+def test_accepts_seeded_low_precision_inputs_exactly():
+    t = make_inputs(1, 2, 33, 8, torch.bfloat16, seed=3)
+    res = oracle.attention(t["q"], t["k"], t["v"], 0.35, dout=t["do"])
+    q = t["q"].double().numpy()
+    assert res["o"].shape == q.shape and res["lse"].shape == q.shape[:-1]
+    # the bf16 values are carried into fp64 without change
+    S = 0.35 * q[0, 1] @ t["k"].double().numpy()[0, 1].T
+    np.testing.assert_allclose(res["lse"][0, 1], scipy.special.logsumexp(S, axis=1), atol=1e-12)
