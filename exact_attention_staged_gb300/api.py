@@ -1,0 +1,213 @@
+"""Python binding of libfa.so: argument marshalling only (ctypes).
+
+Every step of the attention path runs in the library's CUDA kernels; PyTorch supplies device
+memory and the current stream.  There is no fallback: when libfa.so is missing or the device
+is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_FP16, FA_BF16 = 0, 1
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, -1, -2, -3, -4
+
+# exported names and their signatures, in the order include/fa.h declares them
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i,
+                    _f, _i, _vp, _vp]),
+    "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "fa_bwd_dkdv": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
+                         _vp, _vp]),
+    "fa_bwd_dq": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_sync_status": (_i, [_vp]),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_debug_set_visit_log": (_i, [_vp, _sz]),
+    "fa_debug_set_wait_limit_ns": (_i, [ctypes.c_ulonglong]),
+    "fa_debug_set_fault": (_i, [_i]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def load(path: str = LIB_PATH):
+    """Load libfa.so (built by ``exact_attention_staged_gb300.build``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m exact_attention_staged_gb300.build`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != FA_OK:
+        raise FAError(code, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float16")
+
+
+def _dev(t: Optional[torch.Tensor], name: str, like: Optional[torch.Tensor] = None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if like is not None and (t.shape != like.shape or t.dtype != like.dtype):
+        raise ValueError(f"{name} must match q in shape and dtype")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _shape(q: torch.Tensor):
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def fwd(q, k, v, scale: Optional[float] = None, causal: bool = False, block_mask=None,
+        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+        stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE = attention forward (fa_fwd, or fa_fwd_blocksparse when block_mask is given)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be fp32 [B, H, N]")
+    args = [_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q), _dev(out, "out", q), _dev(lse, "lse"),
+            B, H, N, d, _dtype_code(q), float(scale), int(bool(causal))]
+    if block_mask is None:
+        _check(lib.fa_fwd(*args, _stream(stream)), "fa_fwd")
+    else:
+        if block_mask.dtype != torch.uint8:
+            raise TypeError("block_mask must be uint8")
+        _check(lib.fa_fwd_blocksparse(*args, _dev(block_mask, "block_mask"), _stream(stream)),
+               "fa_fwd_blocksparse")
+    return out, lse
+
+
+def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def bwd(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool = False,
+        block_mask=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV = attention backward (fa_bwd)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    nbytes = workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_bwd(_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q), _dev(o, "o", q),
+                      _dev(dout, "dout", q), _dev(lse, "lse"), _dev(dq, "dq", q),
+                      _dev(dk, "dk", q), _dev(dv, "dv", q), _dev(workspace, "workspace"),
+                      nbytes, B, H, N, d, _dtype_code(q), float(scale), int(bool(causal)),
+                      mask_ptr, _stream(stream)), "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_preprocess(o, dout, delta, stream=None):
+    B, H, N, d = _shape(o)
+    _check(load().fa_bwd_preprocess(_dev(o, "o"), _dev(dout, "dout", o), _dev(delta, "delta"),
+                                    B, H, N, d, _dtype_code(o), _stream(stream)),
+           "fa_bwd_preprocess")
+    return delta
+
+
+def bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, scale=None, causal=False, block_mask=None,
+             stream=None):
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(load().fa_bwd_dkdv(_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q),
+                              _dev(dout, "dout", q), _dev(lse, "lse"), _dev(delta, "delta"),
+                              _dev(dk, "dk", q), _dev(dv, "dv", q), B, H, N, d, _dtype_code(q),
+                              float(scale), int(bool(causal)), mask_ptr, _stream(stream)),
+           "fa_bwd_dkdv")
+    return dk, dv
+
+
+def bwd_dq(q, k, v, dout, lse, delta, dq, scale=None, causal=False, block_mask=None,
+           stream=None):
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(load().fa_bwd_dq(_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q),
+                            _dev(dout, "dout", q), _dev(lse, "lse"), _dev(delta, "delta"),
+                            _dev(dq, "dq", q), B, H, N, d, _dtype_code(q), float(scale),
+                            int(bool(causal)), mask_ptr, _stream(stream)), "fa_bwd_dq")
+    return dq
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load().fa_sync_status(_stream(stream)))
+
+
+def debug_set_visit_log(buf: Optional[torch.Tensor]):
+    if buf is None:
+        _check(load().fa_debug_set_visit_log(None, 0), "fa_debug_set_visit_log")
+    else:
+        if buf.dtype != torch.uint8:
+            raise TypeError("visit log must be uint8")
+        _check(load().fa_debug_set_visit_log(_dev(buf, "visit_log"), buf.numel()),
+               "fa_debug_set_visit_log")
+
+
+def debug_set_wait_limit_ns(ns: int):
+    _check(load().fa_debug_set_wait_limit_ns(int(ns)), "fa_debug_set_wait_limit_ns")
+
+
+def debug_set_fault(mode: int):
+    _check(load().fa_debug_set_fault(int(mode)), "fa_debug_set_fault")

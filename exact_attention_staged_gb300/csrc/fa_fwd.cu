@@ -1,0 +1,438 @@
+// fa_fwd.cu - fused exact-attention forward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Computes, per (batch, head) and per 128-row query tile Q_i, the FlashAttention-2 forward
+// ("FlashAttention-2: better parallelism and work partitioning" reading notes, Algorithm 1):
+// S_ij = Q_i K_j^T on the tensor cores into tensor memory, the online softmax statistics
+// (m, l) in fp32 with one thread per row, P~_ij = exp(S_ij - m) rounded to the input type,
+// O~_i += P~_ij V_j on the tensor cores, and once per row O_i = O~_i / l_i and
+// L_i = m_i + ln(l_i) (delayed normalisation eq. (10)-(11), logsumexp eq. (15)).  Neither S nor
+// P ever leaves the SM.  Causal tiles above the diagonal and tiles whose block-mask entry is
+// zero are never loaded nor multiplied (FlashAttention-2 notes, causal masking section;
+// FlashAttention post, "Block-Sparse FlashAttention").
+//
+// GB300 mapping (prior art on the pages is A100 mma.sync with warp split-Q; not used here):
+//   CTA = two query tiles of one head (256 rows), 320 threads, one CTA per SM:
+//     warp 0       TMA producer: Q tiles once, then K_j and V_j into a ring of smem slots
+//     warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS), O_t += P_t V_j (TS, P in TMEM)
+//     warps 2..5   softmax for query tile 0, one TMEM lane (= query row) per thread
+//     warps 6..9   softmax for query tile 1
+//   TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
+//   P_t is written as packed 16-bit pairs over the first 64 columns of S_t and read from
+//   there by the PV MMA, so P never touches shared memory.
+//   MMA issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j): while one softmax
+//   group exponentiates, the tensor core works on the other group's products.
+//   The running max is kept in log2 units; O and l are rescaled only when the max grows by more
+//   than 8 (a factor 256).  This is exact: O~ and l always share the same reference max, and the
+//   final O~/l and L = m + log2(l) (converted to natural log) do not depend on which max it is.
+#include "fa_internal.h"
+
+#include <cmath>
+#include <type_traits>
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdLayout {
+    static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d tile of 16-bit values
+    static constexpr int kBoxes = D / 64;             // 128-byte-wide TMA boxes per tile row
+    static constexpr int kBoxBytes = kTile * 128;     // 16 KB
+    static constexpr int kSlots = (D == 128) ? 4 : 8; // K/V ring slots
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+    // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], drain
+    static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+    static constexpr int kThreads = 320;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    const uint32_t a = smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+__device__ __forceinline__ bool tile_live(const FwdParams &p, int qt, int j) {
+    if (qt >= p.T) return false;
+    if (p.causal && j > qt) return false;
+    if (p.mask != nullptr && p.mask[qt * p.T + j] == 0) return false;
+    return true;
+}
+
+// Bounded wait that ignores the abort flag: used only to drain copies and MMAs in flight.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (global_timer_ns() - t0 > ctl.wait_limit_ns) return;
+    }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+    using L = FwdLayout<D>;
+    constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, true);
+    constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *full = bars + 1;
+    uint64_t *empty = full + L::kSlots;
+    uint64_t *s_full = empty + L::kSlots;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_final = p_full + 2;
+    uint64_t *drain = o_final + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+
+    const int warp = warp_id(), lane = lane_id();
+    const int bh = blockIdx.x % p.BH;
+    const int pair = p.num_pairs - 1 - static_cast<int>(blockIdx.x / p.BH);  // long rows first
+    const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+    const bool has1 = qt1 < p.T;
+    const int jend = p.causal ? min(has1 ? qt1 : qt0, p.T - 1) + 1 : p.T;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < L::kSlots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_final[t], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint8_t *sQ = smem + L::kQOff;
+            mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
+            for (int t = 0; t < (has1 ? 2 : 1); ++t)
+                for (int b = 0; b < L::kBoxes; ++b)
+                    tma_load_3d(sQ + t * L::kTileBytes + b * L::kBoxBytes, &tmq, b * 64,
+                                (qt0 + t) * kTile, bh, q_full);
+            int n = 0;
+            bool ok = true;
+            for (int j = 0; j < jend && ok; ++j) {
+                if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int s = n % L::kSlots;
+                    const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
+                    if (!mbar_wait(&empty[s], par, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!(p.ctl.fault_mode == 1 && n == 0)) {
+                        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+                        uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
+                        for (int b = 0; b < L::kBoxes; ++b)
+                            tma_load_3d(dst + b * L::kBoxBytes, kv ? &tmv : &tmk, b * 64,
+                                        j * kTile, bh, &full[s]);
+                    }
+                    ++n;
+                }
+            }
+            if (!ok || *abort_flag) {
+                // let every copy still in flight land before the CTA's shared memory goes away
+                drain_wait(q_full, 0, p.ctl);
+                const int first = n > L::kSlots ? n - L::kSlots : 0;
+                for (int l = first; l < n; ++l) {
+                    if (p.ctl.fault_mode == 1 && l == 0) continue;
+                    drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t sQ = smem_u32(smem + L::kQOff);
+            const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
+            bool ok = mbar_wait(q_full, 0, p.ctl, abort_flag);
+            tc_fence_after();
+            int n = 0;
+            int cnt[2] = {0, 0};
+            int prev_j = -1;
+            bool prev_live[2] = {false, false};
+            int prev_vs = 0;
+            uint32_t prev_vpar = 0;
+
+            auto issue_s = [&](int t, int ks) {
+                const uint32_t a0 = sQ + t * L::kTileBytes;
+                const uint32_t b0 = sSlots + ks * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    umma_ss(tmem + t * 128, sdesc_sw128(a0 + off, 16, 1024),
+                            sdesc_sw128(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool accumulate) {
+                const uint32_t b0 = sSlots + vs * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk) {
+                    umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+                            sdesc_sw128(b0 + kk * 2048, L::kBoxBytes, 1024), kIdescPV,
+                            (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            for (int j = 0; ok && j < jend; ++j) {
+                const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
+                if (!lv[0] && !lv[1]) continue;
+                const int ks = n % L::kSlots;
+                const uint32_t kpar = (n / L::kSlots) & 1;
+                const int vs = (n + 1) % L::kSlots;
+                const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
+                if (!mbar_wait(&full[ks], kpar, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool v_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (prev_j >= 0 && prev_live[t]) {
+                        if (!v_ready) {
+                            if (!mbar_wait(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        if (!mbar_wait(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, prev_vs, cnt[t] > 0);
+                        ++cnt[t];
+                    }
+                    if (lv[t]) {
+                        issue_s(t, ks);
+                        umma_commit(&s_full[t]);
+                        if (p.ctl.visit_log != nullptr)
+                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
+                                            j] |= 1;
+                    }
+                }
+                if (!ok) break;
+                if (prev_j >= 0) umma_commit(&empty[prev_vs]);
+                umma_commit(&empty[ks]);
+                prev_j = j;
+                prev_live[0] = lv[0];
+                prev_live[1] = lv[1];
+                prev_vs = vs;
+                prev_vpar = vpar;
+                n += 2;
+            }
+            if (ok && prev_j >= 0) {
+                bool v_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (!prev_live[t]) continue;
+                    if (!v_ready) {
+                        ok = mbar_wait(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
+                        v_ready = true;
+                        if (!ok) break;
+                    }
+                    if (!mbar_wait(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(t, prev_vs, cnt[t] > 0);
+                    ++cnt[t];
+                }
+                if (ok) umma_commit(&empty[prev_vs]);
+            }
+            if (ok) {
+                for (int t = 0; t < 2; ++t)
+                    if (cnt[t] > 0) umma_commit(&o_final[t]);
+            }
+            // every MMA issued above completes before the CTA releases TMEM and smem
+            umma_commit(drain);
+            drain_wait(drain, 0, p.ctl);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- softmax groups
+        const int t = (warp - 2) >> 2;
+        const int quad = warp & 3;  // a warp may touch TMEM lanes [32*(warp%4), +32)
+        const int row = quad * 32 + lane;
+        const int qt = t == 0 ? qt0 : qt1;
+        const int q_row = qt * kTile + row;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + t * 128;
+        const uint32_t tO = tmem + lane_base + 256 + t * D;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY;  // running (reference) max of the scaled scores, log2 units
+        float l = 0.f;        // running sum of exp2(score - m)
+        int cnt = 0;
+        bool ok = true;
+        for (int j = 0; j < jend; ++j) {
+            if (!tile_live(p, qt, j)) continue;
+            if (!mbar_wait_warp(&s_full[t], cnt & 1, p.ctl, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[128];
+            tmem_ld32(tS + 0, r + 0);
+            tmem_ld32(tS + 32, r + 32);
+            tmem_ld32(tS + 64, r + 64);
+            tmem_ld32(tS + 96, r + 96);
+            tmem_wait_ld();
+            const int kv0 = j * kTile;
+            const bool need_mask = (p.causal && j == qt) || (kv0 + kTile > p.N);
+            float mx = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int col = kv0 + c;
+                    if (col >= p.N || (p.causal && col > q_row)) r[c] = __float_as_uint(-INFINITY);
+                    mx = fmaxf(mx, __uint_as_float(r[c]));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c]));
+            }
+            const float m_tile = mx * sl2;
+            const float m_new = fmaxf(m, m_tile);
+            const bool old_finite = m != -INFINITY;
+            const bool grow = m_new > m + 8.0f;
+            float alpha = 1.f;
+            if (grow) {
+                if (old_finite) alpha = ex2(m - m_new);
+                l *= alpha;
+                m = m_new;
+            }
+            const bool rescale = grow && old_finite;
+            const float mu = m == -INFINITY ? 0.f : m;  // a row with nothing unmasked yet
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float a = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c]), sl2, -mu));
+                    const float b = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c + 1]), sl2, -mu));
+                    rs0 += a;
+                    rs1 += b;
+                    pk[c] = pack2<BF16>(a, b);
+                }
+                tmem_st32(tS + 32 * h, pk);
+            }
+            l += rs0 + rs1;
+            if (__any_sync(0xffffffffu, rescale)) {
+                // The previous PV into O_t has completed (its commit preceded this S_t) and the
+                // next one waits for p_full, so O_t is ours to rescale here.
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + cc * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+            ++cnt;
+        }
+        if (ok && cnt > 0) {
+            ok = mbar_wait_warp(&o_final[t], 0, p.ctl, abort_flag);
+            tc_fence_after();
+        }
+        if (ok) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool valid = q_row < p.N;
+            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+            T *orow = reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.N + q_row) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                if (cnt > 0) {
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv,
+                                       __uint_as_float(o[2 * e + 1]) * inv);
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+            if (valid)
+                p.lse[static_cast<size_t>(bh) * p.N + q_row] =
+                    l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const Maps &maps, const FwdParams &p, cudaStream_t stream) {
+    using L = FwdLayout<D>;
+    auto kern = fa_fwd_kernel<D, BF16>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    const long grid = static_cast<long>(p.BH) * p.num_pairs;
+    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(maps.q, maps.k, maps.v,
+                                                                           p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Maps &maps, const FwdParams &p, int d, bool bf16,
+                       cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_fwd_t<64, true>(maps, p, stream)
+                             : launch_fwd_t<64, false>(maps, p, stream);
+    return bf16 ? launch_fwd_t<128, true>(maps, p, stream)
+                : launch_fwd_t<128, false>(maps, p, stream);
+}
+
+}  // namespace fa

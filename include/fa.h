@@ -1,0 +1,141 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) fused exact-attention library, libfa.so.
+ *
+ * Computes O = softmax(scale * Q K^T [+ causal or 128x128 block mask]) V without writing the
+ * N x N score or probability matrices to memory, plus its gradient.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layout    Q, K, V, O, dO, dQ, dK, dV are dense, contiguous [B, H, N, d] tensors of one
+ *            16-bit type (FA_FP16 or FA_BF16) in device memory; row (b, h, n) starts at element
+ *            ((b * H + h) * N + n) * d.  LSE and the backward scratch D are fp32 [B, H, N].
+ *            Every device pointer must be 16-byte aligned.
+ *  Sizes     d is 64 or 128 (anything else: FA_ERR_UNSUPPORTED).  N >= 1 (ragged N is fine),
+ *            B >= 1, H >= 1, B * H * N < 2^31.  scale must be finite and > 0.
+ *  Masks     causal != 0: query i sees keys j <= i (queries and keys share one index).
+ *            block_mask: device uint8 [T][T] row-major with T = ceil(N / 128), shared by every
+ *            (b, h); entry (i, j) != 0 keeps the 128 x 128 score block of query rows
+ *            [128 i, 128 i + 128) and key rows [128 j, 128 j + 128).  With both, a score is kept
+ *            only if both keep it.  A query row whose every key is masked gets O = 0,
+ *            LSE = -inf and zero gradients.
+ *  Ownership The caller owns every buffer.  The library allocates no device memory on any
+ *            call; it keeps one device status word per device, created on first use.
+ *  Streams   Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy default
+ *            stream) and returns.  The return code covers argument validation and launch
+ *            errors only.  Device-side failures (a pipeline wait that ran out of time) are
+ *            recorded in the status word and reported by fa_sync_status().
+ *  Errors    0 on success, a negative FA_ERR_* code otherwise; nothing is launched when
+ *            validation fails.  fa_status_string() names a code.
+ *
+ * The operation is the one defined by the pages this library follows:
+ *  - "FlashAttention-2: better parallelism and work partitioning" (reading notes,
+ *    zhongzhuzhou.org): standard attention eq. (2)-(4); forward Algorithm 1 with delayed
+ *    normalisation eq. (10)-(11) and the logsumexp eq. (15); backward Algorithm 2 with
+ *    P = exp(S - L) eq. (16) and the softmax Jacobian eq. (17); causal masking section.
+ *  - FlashAttention post (bluuewhale.github.io): the 1/sqrt(d) scale ("How Attention Is
+ *    Computed") and block-sparse FlashAttention ("Block-Sparse FlashAttention").
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+enum {
+    FA_OK = 0,
+    FA_ERR_INVALID = -1,      /* null or misaligned pointer, bad size, bad scale */
+    FA_ERR_UNSUPPORTED = -2,  /* head dimension other than 64/128, or no sm_103 device */
+    FA_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, attribute, symbol) */
+    FA_ERR_TIMEOUT = -4       /* a device pipeline wait ran out of time (from fa_sync_status) */
+};
+
+/*
+ * Forward.  FlashAttention-2 reading notes, Algorithm 1 (forward) and eq. (15).
+ *   q, k, v : [B,H,N,d] inputs (device).
+ *   o       : [B,H,N,d] output (device), same dtype.
+ *   lse     : [B,H,N] fp32 output (device): LSE_i = m_i + ln(l_i) of the scaled scores.
+ *   scale   : multiplies Q K^T before the softmax (1/sqrt(d) for standard attention).
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+           int d, int dtype, float scale, int causal, void *stream);
+
+/*
+ * Block-sparse forward.  FlashAttention post, "Block-Sparse FlashAttention": a 128 x 128 score
+ * block whose mask entry is zero is skipped entirely (never loaded, never multiplied).
+ *   block_mask : device uint8 [ceil(N/128)][ceil(N/128)], must not be NULL.
+ * Other arguments as fa_fwd.
+ */
+int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int H, int N, int d, int dtype, float scale, int causal,
+                       const uint8_t *block_mask, void *stream);
+
+/* Bytes of device scratch fa_bwd needs: D (fp32 [B,H,N]), rounded up to 256 bytes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward.  FlashAttention-2 reading notes, Algorithm 2 with the atomic dQ update replaced by
+ * a separate dQ pass: D = rowsum(dO o O) (fa_bwd_preprocess), then dK and dV per key tile
+ * (fa_bwd_dkdv), then dQ per query tile (fa_bwd_dq).  Deterministic: no atomics.
+ *   o, lse     : the forward's outputs for these q, k, v (same scale, causal, mask).
+ *   dout       : [B,H,N,d] gradient of the loss with respect to O.
+ *   dq, dk, dv : [B,H,N,d] outputs (device), same dtype as q.
+ *   workspace  : device scratch of at least fa_bwd_workspace_bytes() bytes, 16-byte aligned;
+ *                overwritten, needs no initialisation.
+ *   block_mask : NULL for dense, otherwise as in fa_fwd_blocksparse.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+           const float *lse, void *dq, void *dk, void *dv, void *workspace,
+           size_t workspace_bytes, int B, int H, int N, int d, int dtype, float scale,
+           int causal, const uint8_t *block_mask, void *stream);
+
+/*
+ * The three stages of fa_bwd, exposed so a caller (or a profiler) can order or time them.
+ * fa_bwd_preprocess: delta[b,h,i] = sum_k dout[b,h,i,k] * o[b,h,i,k] in fp32 (FlashAttention-2
+ *   reading notes, Algorithm 2, precomputation; FlashAttention paper detail, "Technique 2").
+ * fa_bwd_dkdv: dK, dV for every key tile from q, k, v, dout, lse and delta.
+ * fa_bwd_dq:   dQ for every query tile from q, k, v, dout, lse and delta.
+ */
+int fa_bwd_preprocess(const void *o, const void *dout, float *delta, int B, int H, int N, int d,
+                      int dtype, void *stream);
+int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dout, const float *lse,
+                const float *delta, void *dk, void *dv, int B, int H, int N, int d, int dtype,
+                float scale, int causal, const uint8_t *block_mask, void *stream);
+int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
+              const float *delta, void *dq, int B, int H, int N, int d, int dtype, float scale,
+              int causal, const uint8_t *block_mask, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status word:
+ * FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a pipeline wait and returned early; its outputs
+ * are undefined) or FA_ERR_CUDA (the stream reported an error).
+ */
+int fa_sync_status(void *stream);
+
+/* Static string naming a return code. */
+const char *fa_status_string(int code);
+
+/*
+ * Test and diagnostics hooks (process-wide; they affect launches made after the call).
+ * fa_debug_set_visit_log: when buf != NULL, every kernel ORs a bit into
+ *   buf[((b*H + h) * T + i) * T + j] for each score tile (query tile i, key tile j) it
+ *   computes: bit 0 forward, bit 1 dK/dV, bit 2 dQ.  bytes must cover B*H*T*T of the launches
+ *   that follow.  NULL turns logging off.
+ * fa_debug_set_wait_limit_ns: bound on every device pipeline wait (default 2 s; 0 restores it).
+ * fa_debug_set_fault: 0 = none; 1 = the forward's load warp skips the first key tile of each
+ *   CTA, so the bounded waits run out and fa_sync_status() reports FA_ERR_TIMEOUT.
+ */
+int fa_debug_set_visit_log(uint8_t *buf, size_t bytes);
+int fa_debug_set_wait_limit_ns(unsigned long long ns);
+int fa_debug_set_fault(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,85 @@
+"""The C-ABI library: it loads, exports every function include/fa.h declares, and rejects bad
+arguments on the host before touching a device (CPU only, no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_staged_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(fa_[a-z0-9_]+)\s*\(",
+                      text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("fa_fwd", "fa_fwd_blocksparse", "fa_bwd", "fa_bwd_workspace_bytes",
+                     "fa_sync_status", "fa_status_string"):
+        assert required in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = header_functions()
+    for n in names:
+        assert hasattr(lib, n), n
+    # the binding wraps exactly the declared set
+    assert set(api.SIGNATURES) == set(names)
+
+
+def test_status_strings_and_workspace_size(lib):
+    assert api.status_string(0) == "ok"
+    assert "timed out" in api.status_string(api.FA_ERR_TIMEOUT)
+    assert api.status_string(12345) == "unknown status"
+    assert api.workspace_bytes(1, 1, 1, 64) == 256
+    assert api.workspace_bytes(2, 16, 4096, 128) == 2 * 16 * 4096 * 4
+    assert api.workspace_bytes(1, 1, 100, 64) == 512
+    assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, H=1, N=128, d=64, dt=1, scale=0.125, causal=0):
+    p = [ctypes.c_void_p(x) if x else None for x in (q, k, v, o, lse)]
+    return lib.fa_fwd(*p, B, H, N, d, dt, scale, causal, None)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # invalid arguments are refused on the host; these calls never reach a device
+    assert _fwd(lib, q=0) == api.FA_ERR_INVALID            # null pointer
+    assert _fwd(lib, k=8) == api.FA_ERR_INVALID            # misaligned pointer
+    assert _fwd(lib, N=0) == api.FA_ERR_INVALID
+    assert _fwd(lib, B=0) == api.FA_ERR_INVALID
+    assert _fwd(lib, dt=7) == api.FA_ERR_INVALID
+    assert _fwd(lib, scale=0.0) == api.FA_ERR_INVALID
+    assert _fwd(lib, scale=float("nan")) == api.FA_ERR_INVALID
+    assert _fwd(lib, d=96) == api.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, B=1 << 16, H=1 << 16) == api.FA_ERR_INVALID  # B*H*N overflows
+    p = ctypes.c_void_p(16)
+    assert lib.fa_fwd_blocksparse(p, p, p, p, p, 1, 1, 128, 64, 1, 0.125, 0, None,
+                                  None) == api.FA_ERR_INVALID  # block mask required
+    assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 128, 64, 1, 0.125, 0, None,
+                      None) == api.FA_ERR_INVALID  # workspace too small
+    assert lib.fa_debug_set_fault(5) == api.FA_ERR_INVALID
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = api._lib
+    api._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            api.load(str(tmp_path / "libfa.so"))
+    finally:
+        api._lib = saved

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element by element.
+
+Tolerances (fixed for this method):
+  O      max |O - O_ref| <= 2e-2 and ||O - O_ref||_F / ||O_ref||_F <= 5e-3
+  LSE    max |LSE - LSE_ref| <= 1e-3
+  dQ, dK, dV   ||x - x_ref||_F / ||x_ref||_F <= 1e-2
+  tile skipping (which score tiles each kernel computes): bit-exact
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_staged_gb300.workloads import (BLOCK, WORKLOADS, make_block_mask,
+                                                    make_inputs, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_REL, LSE_MAX, G_REL = 2e-2, 5e-3, 1e-3, 1e-2
+DEV = "cuda:0"
+
+
+def relf(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def np64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def check_fwd(o, lse, ref, what=""):
+    o, lse = np64(o), np64(lse)
+    err = float(np.max(np.abs(o - ref["o"])))
+    rel = relf(o, ref["o"])
+    fin = np.isfinite(ref["lse"])
+    assert np.array_equal(np.isneginf(lse), ~fin), f"{what}: -inf LSE rows differ"
+    lerr = float(np.max(np.abs(lse[fin] - ref["lse"][fin]))) if fin.any() else 0.0
+    assert err <= O_MAX and rel <= O_REL, f"{what}: O maxabs {err:.3e} relF {rel:.3e}"
+    assert lerr <= LSE_MAX, f"{what}: LSE maxabs {lerr:.3e}"
+
+
+def check_bwd(grads, ref, what=""):
+    for name, g in zip(("dq", "dk", "dv"), grads):
+        r = relf(np64(g), ref[name])
+        assert r <= G_REL, f"{what}: {name} relF {r:.3e}"
+
+
+def run_pair(api, t, scale, causal, mask=None, backward=True):
+    q, k, v, do = (t[x].to(DEV) for x in ("q", "k", "v", "do"))
+    m = None if mask is None else mask.to(DEV)
+    o, lse = api.fwd(q, k, v, scale, causal=causal, block_mask=m)
+    grads = api.bwd(q, k, v, o, lse, do, scale, causal=causal, block_mask=m) if backward else None
+    assert api.sync_status() == 0
+    return o, lse, grads
+
+
+SMALL = [(n, d) for d in (64, 128) for n in (1, 17, 128, 200, 256, 384, 513)]
+
+
+@pytest.mark.parametrize("N,d", SMALL)
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_shapes_bf16(cuda_lib, N, d, causal):
+    t = make_inputs(1, 2, N, d, torch.bfloat16, seed=100 + N + d)
+    scale = 1 / math.sqrt(d)
+    o, lse, grads = run_pair(cuda_lib, t, scale, causal)
+    ref = oracle.attention(t["q"], t["k"], t["v"], scale, causal, dout=t["do"])
+    check_fwd(o, lse, ref, f"N={N} d={d} causal={causal}")
+    check_bwd(grads, ref, f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("N,d", [(128, 64), (300, 128), (640, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_shapes_fp16(cuda_lib, N, d, causal):
+    t = make_inputs(2, 1, N, d, torch.float16, seed=200 + N)
+    scale = 1 / math.sqrt(d)
+    o, lse, grads = run_pair(cuda_lib, t, scale, causal)
+    ref = oracle.attention(t["q"], t["k"], t["v"], scale, causal, dout=t["do"])
+    check_fwd(o, lse, ref, f"fp16 N={N} d={d} causal={causal}")
+    check_bwd(grads, ref, f"fp16 N={N} d={d} causal={causal}")
+
+
+def test_wide_scores_and_odd_scale(cuda_lib):
+    # scores of std ~8 make the running max move often (many rescales of O and l)
+    t = make_inputs(1, 2, 700, 128, torch.bfloat16, seed=7, qk_mult=2.0)
+    o, lse, grads = run_pair(cuda_lib, t, 0.17, True)
+    ref = oracle.attention(t["q"], t["k"], t["v"], 0.17, True, dout=t["do"])
+    check_fwd(o, lse, ref, "wide")
+    check_bwd(grads, ref, "wide")
+
+
+@pytest.mark.parametrize("N,d,causal,seed", [(640, 64, False, 1), (640, 128, True, 2),
+                                             (1000, 64, True, 3), (1000, 128, False, 4)])
+def test_block_sparse_small(cuda_lib, N, d, causal, seed):
+    T = (N + BLOCK - 1) // BLOCK
+    mask = make_block_mask(T, seed, 0.4, keep_diagonal=(seed % 2 == 0))
+    mask[1, :] = 0  # one query block with no key at all: O = 0, LSE = -inf, zero gradients
+    t = make_inputs(1, 2, N, d, torch.bfloat16, seed=300 + seed)
+    scale = 1 / math.sqrt(d)
+    o, lse, grads = run_pair(cuda_lib, t, scale, causal, mask)
+    ref = oracle.attention(t["q"], t["k"], t["v"], scale, causal, mask, dout=t["do"])
+    check_fwd(o, lse, ref, "sparse")
+    check_bwd(grads, ref, "sparse")
+    assert torch.all(o[:, :, 128:256].cpu() == 0)
+    assert torch.all(grads[0][:, :, 128:256].cpu() == 0)
+
+
+def expected_visits(BH, T, causal, mask):
+    i = np.arange(T)
+    live = np.ones((T, T), dtype=bool)
+    if causal:
+        live &= i[None, :] <= i[:, None]
+    if mask is not None:
+        live &= mask.numpy().astype(bool)
+    return np.broadcast_to(live.astype(np.uint8) * 7, (BH, T, T)).copy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("sparse", [False, True])
+def test_tile_skipping_is_bit_exact(cuda_lib, causal, sparse):
+    B, H, N, d = 1, 3, 1100, 64
+    T = (N + BLOCK - 1) // BLOCK
+    mask = make_block_mask(T, 9, 0.3) if sparse else None
+    t = make_inputs(B, H, N, d, torch.bfloat16, seed=9)
+    log = torch.zeros(B * H * T * T, dtype=torch.uint8, device=DEV)
+    cuda_lib.debug_set_visit_log(log)
+    try:
+        run_pair(cuda_lib, t, 0.125, causal, mask)
+    finally:
+        cuda_lib.debug_set_visit_log(None)
+    got = log.cpu().numpy().reshape(B * H, T, T)
+    assert np.array_equal(got, expected_visits(B * H, T, causal, mask))
+
+
+def test_dead_key_blocks_are_never_read(cuda_lib):
+    # key block 2 is masked for every query block: NaNs there must not reach any output
+    N, d = 768, 128
+    T = N // BLOCK
+    mask = torch.ones(T, T, dtype=torch.uint8)
+    mask[:, 2] = 0
+    t = make_inputs(1, 2, N, d, torch.bfloat16, seed=21)
+    clean = run_pair(cuda_lib, t, 0.1, False, mask)
+    p = dict(t)
+    p["k"] = t["k"].clone()
+    p["v"] = t["v"].clone()
+    p["k"][:, :, 256:384] = float("nan")
+    p["v"][:, :, 256:384] = float("nan")
+    dirty = run_pair(cuda_lib, p, 0.1, False, mask)
+    assert torch.equal(clean[0], dirty[0]) and torch.equal(clean[1], dirty[1])
+    for a, b in zip(clean[2], dirty[2]):
+        assert torch.equal(a, b)
+
+
+def test_deterministic(cuda_lib):
+    t = make_inputs(2, 2, 900, 128, torch.bfloat16, seed=31)
+    a = run_pair(cuda_lib, t, 0.09, True)
+    b = run_pair(cuda_lib, t, 0.09, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for x, y in zip(a[2], b[2]):
+        assert torch.equal(x, y)
+
+
+def test_backward_stages_match_fused_call(cuda_lib):
+    t = make_inputs(1, 2, 500, 64, torch.bfloat16, seed=41)
+    q, k, v, do = (t[x].to(DEV) for x in ("q", "k", "v", "do"))
+    o, lse = cuda_lib.fwd(q, k, v, 0.125, causal=True)
+    dq, dk, dv = cuda_lib.bwd(q, k, v, o, lse, do, 0.125, causal=True)
+    delta = torch.empty_like(lse)
+    cuda_lib.bwd_preprocess(o, do, delta)
+    dk2, dv2 = cuda_lib.bwd_dkdv(q, k, v, do, lse, delta, torch.empty_like(q),
+                                 torch.empty_like(q), 0.125, True)
+    dq2 = cuda_lib.bwd_dq(q, k, v, do, lse, delta, torch.empty_like(q), 0.125, True)
+    assert cuda_lib.sync_status() == 0
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    ref = oracle.attention(t["q"], t["k"], t["v"], 0.125, True, dout=t["do"])
+    # D = rowsum(dO o O) from the kernel's own O agrees with the oracle's <P, dP>
+    assert float(np.max(np.abs(np64(delta) - ref["delta"]))) <= 2e-2
+
+
+def test_timeout_is_reported_not_hung(cuda_lib):
+    # the forward's load warp skips its first key tile: every wait on it runs out after 50 ms,
+    # the kernel returns early, and the status word says so; the context stays usable
+    t = make_inputs(1, 1, 256, 64, torch.bfloat16, seed=51)
+    q, k, v = (t[x].to(DEV) for x in ("q", "k", "v"))
+    cuda_lib.debug_set_wait_limit_ns(50_000_000)
+    cuda_lib.debug_set_fault(1)
+    try:
+        cuda_lib.fwd(q, k, v, 0.125)
+        assert cuda_lib.sync_status() == cuda_lib.FA_ERR_TIMEOUT
+    finally:
+        cuda_lib.debug_set_fault(0)
+        cuda_lib.debug_set_wait_limit_ns(0)
+    o, lse = cuda_lib.fwd(q, k, v, 0.125)
+    assert cuda_lib.sync_status() == 0
+    ref = oracle.attention(t["q"], t["k"], t["v"], 0.125)
+    check_fwd(o, lse, ref, "after timeout")
+
+
+def test_invalid_arguments_on_device(cuda_lib):
+    q = torch.zeros(1, 1, 128, 96, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(cuda_lib.FAError) as e:
+        cuda_lib.fwd(q, q, q)
+    assert e.value.code == cuda_lib.FA_ERR_UNSUPPORTED
+    x = torch.zeros(1 * 1 * 128 * 64 + 1, dtype=torch.bfloat16, device=DEV)[1:].view(1, 1, 128, 64)
+    with pytest.raises(cuda_lib.FAError) as e:
+        cuda_lib.fwd(x, x, x)
+    assert e.value.code == cuda_lib.FA_ERR_INVALID
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def _sampled_heads(BH):
+    return sorted({0, BH - 1})
+
+
+@pytest.mark.parametrize("name", ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k",
+                                  "gpt_causal_d128_n8k", "blocksparse_d64_n16k"])
+def test_workload_parity(cuda_lib, name):
+    w = WORKLOADS[name]
+    t = workload_inputs(w)
+    mask = t.get("block_mask")
+    o, lse, grads = run_pair(cuda_lib, t, w.scale, w.causal, mask, backward=w.backward)
+    BH = w.B * w.H
+    flat = {x: t[x].reshape(BH, w.N, w.d) for x in ("q", "k", "v", "do")}
+    for h in _sampled_heads(BH):
+        ref = oracle.attention(flat["q"][h], flat["k"][h], flat["v"][h], w.scale, w.causal,
+                               mask, dout=flat["do"][h] if w.backward else None)
+        check_fwd(o.reshape(BH, w.N, w.d)[h], lse.reshape(BH, w.N)[h], ref, f"{name} head {h}")
+        if w.backward:
+            check_bwd([g.reshape(BH, w.N, w.d)[h] for g in grads], ref, f"{name} head {h}")
+    # every head is finite and LSE never exceeds what its scores allow
+    assert torch.isfinite(o).all()
+    if w.backward:
+        for g in grads:
+            assert torch.isfinite(g).all()
