@@ -1,0 +1,387 @@
+"""Benchmark: exact-attention forward + backward through the C ABI on GB300.
+
+One step = one pass of the whole hot path over one batch: fa_fwd (forward kernel), then the
+backward's three stages (D pre-pass, dK/dV kernel, dQ kernel), on the GPT-style long-context
+training shape (causal, B=1 H=32 N=8192 d=128, bf16, Q and K doubled).  Inputs are resident in
+HBM before timing; the step's working set (Q, K, V, dO, O, dQ, dK, dV: 537 MB) is larger than
+the 129 MB L2, so no flush is done between steps.
+
+FLOP convention (FlashAttention-2 reading notes, reproducibility section): forward 4*N^2*d per
+head, backward 2.5x that, both halved for causal attention.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, no data
+exchange); the time is the max over ranks and the value counts every rank's work.
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample of the same
+workload (one head, its first 4096 query/key rows: a self-contained causal sub-problem).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_attention_staged_gb300.workloads import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
+SAMPLE_ROWS = 4096
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": "exact_attention_staged_gb300/csrc/fa_fwd.cu",
+    "fa_bwd_dkdv_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
+    "fa_bwd_dq_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
+    "fa_bwd_preprocess_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
+}
+
+
+# ------------------------------------------------------------------------------- bookkeeping
+
+def flops(B, H, N, d, causal, density=1.0):
+    """Algorithmic FLOPs per kernel of one step."""
+    f = 4.0 * B * H * N * N * d * (0.5 if causal else 1.0) * density
+    return {"fa_fwd_kernel": f, "fa_bwd_preprocess_kernel": 0.0,
+            "fa_bwd_dkdv_kernel": 2.0 * f, "fa_bwd_dq_kernel": 0.5 * f}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained":
+                p.get("bf16_tflops_sustained", p["bf16_tflops"]), "hbm_gbs": p["hbm_gbs"],
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[workload][kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, rows=SAMPLE_ROWS):
+    """Time the fp64 oracle on one head's first `rows` queries and keys (fwd + bwd)."""
+    import oracle
+    t = workload_inputs(w)
+    n = min(rows, w.N)
+    sl = {x: t[x][0, 0, :n].clone() for x in ("q", "k", "v", "do")}
+    mask = t.get("block_mask")
+    if mask is not None:
+        tiles = (n + 127) // 128
+        mask = mask[:tiles, :tiles].clone()
+    t0 = time.perf_counter()
+    oracle.attention(sl["q"], sl["k"], sl["v"], w.scale, w.causal, mask, dout=sl["do"])
+    dt = time.perf_counter() - t0
+    dens = 1.0 if mask is None else float(mask.float().mean())
+    f = sum(flops(1, 1, n, w.d, w.causal, dens).values())
+    return {"seconds": dt, "flops": f, "rows": n, "cores": oracle.num_threads()}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample(w)
+    total_s, total_f = 0.0, 0.0
+    cores = 1
+    for _ in range(args.steps):
+        r = oracle_sample(w)
+        total_s += r["seconds"]
+        total_f += r["flops"]
+        cores = r["cores"]
+    value = total_f / total_s / 1e12
+    sample = (f"one head, first {min(SAMPLE_ROWS, w.N)} query/key rows of {w.describe()} "
+              f"(a self-contained causal sub-problem), fp64 oracle fwd+bwd per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.describe()},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w):
+    from exact_attention_staged_gb300 import api
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.load()
+    t = workload_inputs(w)
+    mask_cpu = t.get("block_mask")
+    q, k, v, do = (t[x].to(dev) for x in ("q", "k", "v", "do"))
+    mask = None if mask_cpu is None else mask_cpu.to(dev)
+    density = 1.0 if mask_cpu is None else float(mask_cpu.float().mean())
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    delta = torch.empty_like(lse)
+    stream = torch.cuda.current_stream()
+    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel",
+             "fa_bwd_dq_kernel"]
+
+    def step(events=None):
+        def mark(i):
+            if events is not None:
+                events[i].record(stream)
+        mark(0)
+        api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
+        mark(1)
+        api.bwd_preprocess(o, do, delta)
+        mark(2)
+        api.bwd_dkdv(q, k, v, do, lse, delta, dk, dv, w.scale, w.causal, mask)
+        mark(3)
+        api.bwd_dq(q, k, v, do, lse, delta, dq, w.scale, w.causal, mask)
+        mark(4)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error in the timed region")
+    max_ms = dist_max(elapsed_ms, world, dev)
+    f = flops(w.B, w.H, w.N, w.d, w.causal, density)
+    step_flops = sum(f.values())
+    value = world * step_flops * args.steps / (max_ms / 1e3) / 1e12
+    per_kernel = {}
+    for i, n in enumerate(names):
+        ms = [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
+        per_kernel[n] = {"ms": statistics.mean(ms),
+                         "tflops": f[n] / (statistics.mean(ms) / 1e3) / 1e12}
+    fwd_ms = per_kernel["fa_fwd_kernel"]["ms"]
+    bwd_ms = sum(per_kernel[n]["ms"] for n in names[1:])
+    peaks = measured_peaks()
+    dominant = max(names, key=lambda n: per_kernel[n]["ms"])
+    achieved = per_kernel[dominant]["tflops"]
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": ncu_traffic(dominant, w.name),
+                "peak_kind": f"bf16 dense sustained ({peaks['source']})"}
+
+    # ---- end to end through the C ABI from pinned host buffers
+    e2e_steps = max(1, min(args.steps, 5))
+    hq, hk, hv, hdo = (t[x].pin_memory() for x in ("q", "k", "v", "do"))
+    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+    hlse = torch.empty(w.B, w.H, w.N, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hdq, hdk, hdv, hlse))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
+        api.bwd(q, k, v, o, lse, do, w.scale, w.causal, mask, dq=dq, dk=dk, dv=dv,
+                workspace=delta)
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world, dev)
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error in the end-to-end loop")
+    e2e_value = world * step_flops * e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = oracle_sample(w)
+        cpu = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s",
+               "cores": r["cores"], "kind": "oracle",
+               "sample": f"one head, first {r['rows']} query/key rows of the workload, fp64 "
+                         f"fwd+bwd, {r['seconds']:.2f} s"}
+    ws = sum(x.numel() * x.element_size() for x in (q, k, v, do, o, dq, dk, dv))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "block_density": density,
+                   "l2": f"inputs larger than L2 (step working set {ws / 1e6:.0f} MB vs "
+                         f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "fwd": {"tflops": f["fa_fwd_kernel"] / (fwd_ms / 1e3) / 1e12, "ms": fwd_ms,
+                "frac_of_peak": f["fa_fwd_kernel"] / (fwd_ms / 1e3) / 1e12 /
+                peaks["bf16_tflops"], "peak_kind": f"bf16 dense burst ({peaks['source']})"},
+        "bwd": {"tflops": (step_flops - f["fa_fwd_kernel"]) / (bwd_ms / 1e3) / 1e12,
+                "ms": bwd_ms},
+        "frac_of_peak": value / world / peak,
+        "kernels": per_kernel,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
