@@ -39,7 +39,7 @@ from exact_attention_staged_gb300.workloads import WORKLOADS, workload_inputs  #
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
 SAMPLE_ROWS = 4096
-L2_BYTES = 129 * 1024 * 1024
+L2_BYTES = 129e6  # GB300 L2 (129 MB)
 KERNEL_SOURCES = {
     "fa_fwd_kernel": "exact_attention_staged_gb300/csrc/fa_fwd.cu",
     "fa_bwd_dkdv_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
@@ -102,7 +102,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -369,7 +369,7 @@ def run_gpu(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
