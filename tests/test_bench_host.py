@@ -1,0 +1,81 @@
+"""Host-side logic of bench.py on the CPU: the replica launch path at world size 2 (gloo),
+the max-over-ranks reduction, the FLOP bookkeeping and the JSON contract of the oracle arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    w, r, _ = bench.dist_setup()
+    assert (w, r) == (world, rank)
+    bench.dist_barrier(w)
+    m = bench.dist_max(float(rank + 1) * 1.5, w, torch.device("cpu"))
+    out.put((rank, m))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 3.0, 1: 3.0}
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
+    port = free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+           "--workload", "tiny_fwd_fp16", "--steps", "2", "--warmup", "1"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    for key in ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "cpu_baseline", "e2e", "config"):
+        assert key in line
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_flop_convention():
+    f = bench.flops(1, 32, 8192, 128, causal=True)
+    fwd = 4 * 32 * 8192 ** 2 * 128 / 2
+    assert f["fa_fwd_kernel"] == fwd
+    assert f["fa_bwd_dkdv_kernel"] + f["fa_bwd_dq_kernel"] == 2.5 * fwd
+    assert abs(fwd / 1e9 - 549.76) < 0.01  # the 8k causal forward is 549.8 GFLOP
+    g = bench.flops(1, 8, 16384, 64, causal=False, density=0.25)
+    assert g["fa_fwd_kernel"] == 4 * 8 * 16384 ** 2 * 64 * 0.25
+
+
+def test_warmup_floor_is_enforced():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "1"])
