@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
 FA_FP16, FA_BF16 = 0, 1
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, -1, -2, -3, -4
+FA_NOALLOC_MAX_ROWS = 1 << 20  # B*H*N limit of fa_bwd_noalloc
 
 # exported names and their signatures, in the order include/fa.h declares them
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -31,6 +32,8 @@ SIGNATURES = {
     "fa_bwd_dkdv": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
                          _vp, _vp]),
     "fa_bwd_dq": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                            _f, _i, _vp, _vp]),
     "fa_sync_status": (_i, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_debug_set_visit_log": (_i, [_vp, _sz]),

@@ -165,6 +165,24 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
     return make_ctl(status, BH, p->T, &p->ctl);
 }
 
+// Scratch of fa_bwd_noalloc: the D values (one float per query row) of one backward call.
+// Host code must not pass this name to a kernel: on the host it only stands in for the
+// symbol; noalloc_scratch() looks up its device address once per device.
+static __device__ __align__(256) float g_noalloc_delta[FA_NOALLOC_MAX_ROWS];
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(int dev, float **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || p == nullptr)
+            return FA_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -245,6 +263,29 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
     if (rc != FA_OK) return rc;
     if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
     float *delta = static_cast<float *>(workspace);
+    rc = fa_bwd_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
+    if (rc != FA_OK) return rc;
+    rc = fa_bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, B, H, N, d, dtype, scale, causal,
+                     block_mask, stream);
+    if (rc != FA_OK) return rc;
+    return fa_bwd_dq(q, k, v, dout, lse, delta, dq, B, H, N, d, dtype, scale, causal, block_mask,
+                     stream);
+}
+
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                   int dtype, float scale, int causal, const uint8_t *block_mask, void *stream) {
+    int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv});
+    if (rc != FA_OK) return rc;
+    if (static_cast<size_t>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID;
+    int dev = 0, *status = nullptr;
+    rc = device_setup(&dev, &status);
+    if (rc != FA_OK) return rc;
+    float *delta = nullptr;
+    rc = noalloc_scratch(dev, &delta);
+    if (rc != FA_OK) return rc;
     rc = fa_bwd_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
     if (rc != FA_OK) return rc;
     rc = fa_bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, B, H, N, d, dtype, scale, causal,

@@ -111,6 +111,30 @@ int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, con
               int causal, const uint8_t *block_mask, void *stream);
 
 /*
+ * Backward that allocates nothing: the same computation, arguments and results as fa_bwd,
+ * without the workspace.  The pages have no counterpart; this entry point serves callers that
+ * cannot allocate device memory themselves, such as a plug-in that a host application hands
+ * only its input and output buffers while the application owns every device allocation, or
+ * code on a latency-critical path where cudaMalloc's implicit device-wide synchronisation is
+ * not acceptable.
+ *
+ * The D scratch lives in a fixed array compiled into libfa.so: FA_NOALLOC_MAX_ROWS floats
+ * (4 MiB) that every GPU which loads the library keeps until the process exits.
+ *  - Returns FA_ERR_INVALID, launching nothing, when B * H * N > FA_NOALLOC_MAX_ROWS.
+ *  - The first call on a device looks up the array's device address with that device current;
+ *    make that first call before any stream capture.
+ *  - Every call on a device uses the same array, which keeps the last call's values.  Calls
+ *    that overlap on the GPU (other streams, other host threads) race on it and corrupt each
+ *    other's gradients: order them.  Nothing in it has to start at zero, since each call
+ *    writes every value it later reads.
+ *  - Neither the call nor its set-up calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define FA_NOALLOC_MAX_ROWS (1u << 20)
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                   int dtype, float scale, int causal, const uint8_t *block_mask, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a pipeline wait and returned early; its outputs
  * are undefined) or FA_ERR_CUDA (the stream reported an error).
