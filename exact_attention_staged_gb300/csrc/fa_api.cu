@@ -107,6 +107,16 @@ int make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int dtype) 
 
 int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 
+// Heads per CTA-order group: the streamed tiles of one head (two [N, d] 16-bit tensors) times
+// the group stay near 32 MiB, a quarter of the L2.
+int head_group(int BH, int N, int d) {
+    const double per_head = 4.0 * N * d;
+    int g = static_cast<int>((32.0 * 1024 * 1024) / per_head);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    return g;
+}
+
 int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                int N, int d, int dtype, float scale, int causal, const uint8_t *mask,
                void *stream) {
@@ -130,6 +140,7 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     p.N = N;
     p.T = tiles_of(N);
     p.num_pairs = (p.T + 1) / 2;
+    p.head_group = head_group(BH, N, d);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
     if (make_ctl(status, BH, p.T, &p.ctl) != FA_OK) return FA_ERR_INVALID;
@@ -159,6 +170,7 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
     p->BH = BH;
     p->N = N;
     p->T = tiles_of(N);
+    p->head_group = head_group(BH, N, d);
     p->scale = scale;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->causal = causal ? 1 : 0;

@@ -19,8 +19,8 @@
 //   dQ           CTA = one 128-row query tile i.  For every live key tile j:
 //                  S = Q_i K_j^T, dP = dO_i V_j^T, P = exp2(...), dS = P o (dP - D_i),
 //                  dQ += dS K_j (TS MMA), and finally dQ *= scale.
-// TMEM (512 columns): [0,128) S or S^T (then P / dS packed over its first 64 columns),
-// [128,256) dP or dP^T (dS^T packed over its first 64 columns), then the d-wide accumulators.
+// In both, two groups of four warps split every 128 x 128 score tile into two 64-wide halves
+// and alternate on the tensor core, the way the forward's two query tiles do.
 #include "fa_internal.h"
 
 #include <cmath>
@@ -103,6 +103,13 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
 }
 
 // ================================================================================ dK / dV
+// CTA = one 128-row key tile, 320 threads: warp 0 loads, warp 1 issues MMAs, warps 2..5
+// (group 0) and 6..9 (group 1) each own one 64-query half of every 128 x 128 score tile.
+// TMEM: S^T half h at [64h, 64h+64), dP^T half h at [128+64h, ...), dV at [256, 256+d),
+// dK at [256+d, 256+2d).  P^T_h and dS^T_h are packed over the first 32 columns of S^T_h and
+// dP^T_h.  MMA order per query tile n (next tile n+1), for h = 0, 1:
+//   dV += P^T_h dO_h;  dK += dS^T_h Q_h;  S^T_h(n+1);  dP^T_h(n+1)
+// so while one group exponentiates, the tensor core works on the other group's half.
 template <int D>
 struct DkvLayout {
     static constexpr int kTileBytes = kTile * D * 2;
@@ -115,40 +122,42 @@ struct DkvLayout {
     // per stage: Q tile, dO tile, then 128 floats of L*log2e and 128 floats of D
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // kv_full, full[S], empty[S], s_full, p_ready, ds_ready, final, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 5;
+    // kv_full, full[S], empty[S], s_full[2], dp_full[2], p_ready[2], ds_ready[2], final, drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 10;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kMiscOff + 16 + 1024;
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 320;
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
     using L = DkvLayout<D>;
-    constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);
-    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);
+    constexpr uint32_t kIdescSS = idesc_f16(128, 64, BF16, false);  // S^T_h, dP^T_h
+    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);    // dV, dK
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *kv_full = bars;
     uint64_t *full = bars + 1;
     uint64_t *empty = full + L::kStages;
-    uint64_t *s_full = empty + L::kStages;
-    uint64_t *p_ready = s_full + 1;
-    uint64_t *ds_ready = p_ready + 1;
-    uint64_t *fin = ds_ready + 1;
+    uint64_t *s_full = empty + L::kStages;  // [2]
+    uint64_t *dp_full = s_full + 2;         // [2]
+    uint64_t *p_ready = dp_full + 2;        // [2]
+    uint64_t *ds_ready = p_ready + 2;       // [2]
+    uint64_t *fin = ds_ready + 2;
     uint64_t *drain = fin + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = warp_id(), lane = lane_id();
-    const int bh = blockIdx.x % p.BH;
-    const int kt = static_cast<int>(blockIdx.x / p.BH);  // key tile
-    const int i0 = p.causal ? kt : 0;                    // first query tile that can see it
+    const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.T, p.head_group);
+    const int bh = ord.head;
+    const int kt = ord.rank;              // key tile; tile 0 sees the most query tiles when causal
+    const int i0 = p.causal ? kt : 0;     // first query tile that can see it
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -156,9 +165,12 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&full[s], 2);  // TMA bytes + the producer warp's L/D stores
             mbar_init(&empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_ready, 128);
-        mbar_init(ds_ready, 128);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&dp_full[h], 1);
+            mbar_init(&p_ready[h], 128);
+            mbar_init(&ds_ready[h], 128);
+        }
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -231,53 +243,92 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             const uint32_t sK = smem_u32(smem + L::kKOff);
             const uint32_t sV = smem_u32(smem + L::kVOff);
-            const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+            const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
+            auto stage_q = [&](int st) {
+                return smem_u32(smem + L::kStageOff + st * L::kStageBytes);
+            };
+            // S^T_h = K Q_h^T and dP^T_h = V dO_h^T, Q_h / dO_h = query rows [64h, 64h+64)
+            const SDesc dK0 = sdesc_make(sK, 16, 1024), dV0 = sdesc_make(sV, 16, 1024);
+            const SDesc dQk0 = sdesc_make(stage_q(0), 16, 1024);
+            const SDesc dQm0 = sdesc_make(stage_q(0), L::kBoxBytes, 1024);
+            auto issue_sdp = [&](int st, int h) {
+                const uint32_t qoff = st * L::kStageBytes + h * 64 * 128;
+                const SDesc bq = sdesc_add(dQk0, qoff), bdo = sdesc_add(dQk0, qoff + L::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + 64 * h, sdesc_add(dK0, off), sdesc_add(bq, off), kIdescSS,
+                           kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[h]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + 128 + 64 * h, sdesc_add(dV0, off), sdesc_add(bdo, off), kIdescSS,
+                           kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&dp_full[h]);
+            };
+            auto next_live = [&](int i) {
+                for (++i; i < p.T; ++i)
+                    if (tile_live(p, i, kt)) return i;
+                return p.T;
+            };
             bool ok = mbar_wait(kv_full, 0, p.ctl, abort_flag);
+            int i = next_live(i0 - 1);
             int n = 0;
-            for (int i = i0; ok && i < p.T; ++i) {
-                if (!tile_live(p, i, kt)) continue;
+            if (ok && i < p.T) {
+                ok = mbar_wait(&full[0], 0, p.ctl, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sdp(0, 0);
+                    issue_sdp(0, 1);
+                    if (p.ctl.visit_log != nullptr)
+                        p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + i) * p.T + kt] |= 2;
+                }
+            }
+            while (ok && i < p.T) {
                 const int s = n % L::kStages;
-                if (!mbar_wait(&full[s], (n / L::kStages) & 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + L::kStageOff + s * L::kStageBytes);
-                const uint32_t sdO = sQ + L::kTileBytes;
+                const int s2 = (n + 1) % L::kStages;
+                const int nxt = next_live(i);
+                const SDesc bQm = sdesc_add(dQm0, s * L::kStageBytes);
+                const SDesc bdOm = sdesc_add(bQm, L::kTileBytes);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!mbar_wait(&p_ready[h], n & 1, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
-                            kIdescSS, kk > 0 ? 1u : 0u);
-                }
+                    for (int kk = 0; kk < 4; ++kk)  // dV += P^T_h dO_h (K = 64 queries)
+                        mma_ts(tdV, tmem + 64 * h + kk * 8, sdesc_add(bdOm, h * 8192 + kk * 2048),
+                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    if (!mbar_wait(&ds_ready[h], n & 1, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tdP, sdesc_sw128(sV + off, 16, 1024),
-                            sdesc_sw128(sdO + off, 16, 1024), kIdescSS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_h Q_h
+                        mma_ts(tdK, tmem + 128 + 64 * h + kk * 8, sdesc_add(bQm, h * 8192 + kk * 2048),
+                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    if (h == 1) umma_commit(&empty[s]);
+                    if (nxt < p.T) {
+                        if (h == 0) {
+                            if (!mbar_wait(&full[s2], ((n + 1) / L::kStages) & 1, p.ctl,
+                                           abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (p.ctl.visit_log != nullptr)
+                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + nxt) * p.T +
+                                                kt] |= 2;
+                        }
+                        issue_sdp(s2, h);
+                    }
                 }
-                umma_commit(s_full);
-                if (p.ctl.visit_log != nullptr)
-                    p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + i) * p.T + kt] |= 2;
-                if (!mbar_wait(p_ready, n & 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)  // dV += P^T dO
-                    umma_ts(tdV, tS + kk * 8, sdesc_sw128(sdO + kk * 2048, L::kBoxBytes, 1024),
-                            kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
-                if (!mbar_wait(ds_ready, n & 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dS^T Q
-                    umma_ts(tdK, tdP + kk * 8, sdesc_sw128(sQ + kk * 2048, L::kBoxBytes, 1024),
-                            kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
+                i = nxt;
                 ++n;
             }
             if (ok && n > 0) umma_commit(fin);
@@ -286,12 +337,13 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------------- compute group
+        // ---------------------------------------------------------------- compute groups
+        const int h = (warp - 2) >> 2;    // query half of every tile this group owns
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // key row within the tile
         const int k_row = kt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tdP = tS + 128, tdV = tS + 256, tdK = tS + 256 + D;
+        const uint32_t tS = tmem + lane_base + 64 * h, tdP = tS + 128;
         const float sl2 = p.scale_log2;
         int n = 0;
         bool ok = true;
@@ -300,58 +352,62 @@ __global__ void __launch_bounds__(192, 1)
             const int s = n % L::kStages;
             // the stage's L and D values were stored by the producer warp before its arrive
             if (!mbar_wait_warp(&full[s], (n / L::kStages) & 1, p.ctl, abort_flag) ||
-                !mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
+                !mbar_wait_warp(&s_full[h], n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float *sl =
                 reinterpret_cast<const float *>(smem + L::kStageOff + s * L::kStageBytes +
-                                                2 * L::kTileBytes);
+                                                2 * L::kTileBytes) + 64 * h;
             const float *sd = sl + 128;
-            const bool diag = p.causal && i == kt;  // only this tile needs the causal compare
-            uint32_t pk[64];                        // P^T of this row, packed 16-bit pairs
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS + 32 * c, r);
+            // query q sees key k only when k <= q: only the diagonal tile needs the compare
+            const bool diag = p.causal && i == kt;
+            uint32_t pk[32];  // P^T of this row's 64 queries, packed 16-bit pairs
+            {
+                uint32_t r[64];
+                tmem_ld32(tS, r);
+                tmem_ld32(tS + 32, r + 32);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int q0 = 32 * c + 2 * e;
-                    float a = ex2(fmaf(__uint_as_float(r[2 * e]), sl2, -sl[q0]));
-                    float b = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, -sl[q0 + 1]));
-                    if (diag) {  // query q sees key k only when k <= q
-                        if (q0 < row) a = 0.f;
-                        if (q0 + 1 < row) b = 0.f;
+                for (int e = 0; e < 32; ++e) {
+                    const int q0 = 2 * e;
+                    float a = ex2(fmaf(__uint_as_float(r[q0]), sl2, -sl[q0]));
+                    float b = ex2(fmaf(__uint_as_float(r[q0 + 1]), sl2, -sl[q0 + 1]));
+                    if (diag) {
+                        if (64 * h + q0 < row) a = 0.f;
+                        if (64 * h + q0 + 1 < row) b = 0.f;
                     }
-                    pk[16 * c + e] = pack2<BF16>(a, b);
+                    pk[e] = pack2<BF16>(a, b);
                 }
             }
             tmem_st32(tS, pk);
-            tmem_st32(tS + 32, pk + 32);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_ready);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tdP + 32 * c, r);
+            mbar_arrive(&p_ready[h]);
+            if (!mbar_wait_warp(&dp_full[h], n & 1, p.ctl, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t r[64];
+                tmem_ld32(tdP, r);
+                tmem_ld32(tdP + 32, r + 32);
                 tmem_wait_ld();
-                uint32_t w[16];
+                uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int q0 = 32 * c + 2 * e;
-                    const float2 pp = unpack2<BF16>(pk[16 * c + e]);
-                    const float a = pp.x * (__uint_as_float(r[2 * e]) - sd[q0]);
-                    const float b = pp.y * (__uint_as_float(r[2 * e + 1]) - sd[q0 + 1]);
-                    w[e] = pack2<BF16>(a, b);
+                for (int e = 0; e < 32; ++e) {
+                    const int q0 = 2 * e;
+                    const float2 pp = unpack2<BF16>(pk[e]);
+                    w[e] = pack2<BF16>(pp.x * (__uint_as_float(r[q0]) - sd[q0]),
+                                       pp.y * (__uint_as_float(r[q0 + 1]) - sd[q0 + 1]));
                 }
-                tmem_st16(tdP + 16 * c, w);  // over columns already read
+                tmem_st32(tdP, w);  // over columns already read
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(ds_ready);
+            mbar_arrive(&ds_ready[h]);
             ++n;
         }
         if (ok && n > 0) {
@@ -359,25 +415,24 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
         }
         if (ok) {
+            // group 0 writes dV, group 1 writes dK (times the softmax scale)
             const bool valid = k_row < p.N;
             using T = elem_t<BF16>;
-            T *dk = reinterpret_cast<T *>(p.out0) + (static_cast<size_t>(bh) * p.N + k_row) * D;
-            T *dv = reinterpret_cast<T *>(p.out1) + (static_cast<size_t>(bh) * p.N + k_row) * D;
+            T *dst = reinterpret_cast<T *>(h == 0 ? p.out1 : p.out0) +
+                     (static_cast<size_t>(bh) * p.N + k_row) * D;
+            const uint32_t tacc = tmem + lane_base + 256 + h * D;
+            const float mul = h == 0 ? 1.f : p.scale;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t a[32], b[32];
+                uint32_t a[32];
                 if (n > 0) {
-                    tmem_ld32(tdV + 32 * cc, a);
-                    tmem_ld32(tdK + 32 * cc, b);
+                    tmem_ld32(tacc + 32 * cc, a);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
+                    for (int e = 0; e < 32; ++e) a[e] = 0u;
                 }
-                if (valid) {
-                    store_row32<BF16>(dv + 32 * cc, a, 1.f);
-                    store_row32<BF16>(dk + 32 * cc, b, p.scale);
-                }
+                if (valid) store_row32<BF16>(dst + 32 * cc, a, mul);
             }
         }
     }
@@ -391,6 +446,11 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ================================================================================ dQ
+// CTA = one 128-row query tile, 320 threads: warp 0 loads, warp 1 issues MMAs, warps 2..5
+// (group 0) and 6..9 (group 1) each own one 64-key half of every 128 x 128 score tile.
+// TMEM: S half h at [64h, 64h+64), dP half h at [128+64h, ...), dQ at [256, 256+d); dS_h is
+// packed over the first 32 columns of S_h.  MMA order per key tile n (next n+1), h = 0, 1:
+//   dQ += dS_h K_h;  S_h(n+1);  dP_h(n+1)
 template <int D>
 struct DqLayout {
     static constexpr int kTileBytes = kTile * D * 2;
@@ -402,37 +462,39 @@ struct DqLayout {
     static constexpr int kStageOff = 2 * kTileBytes;
     static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, V tile
     static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // q_full, full[S], empty[S], s_full, ds_ready, final, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 4;
+    // q_full, full[S], empty[S], s_full[2], dp_full[2], ds_ready[2], final, drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kMiscOff + 16 + 1024;
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 320;
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
     using L = DqLayout<D>;
-    constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);
-    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);
+    constexpr uint32_t kIdescSS = idesc_f16(128, 64, BF16, false);  // S_h, dP_h
+    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);    // dQ
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *full = bars + 1;
     uint64_t *empty = full + L::kStages;
-    uint64_t *s_full = empty + L::kStages;
-    uint64_t *ds_ready = s_full + 1;
-    uint64_t *fin = ds_ready + 1;
+    uint64_t *s_full = empty + L::kStages;  // [2]
+    uint64_t *dp_full = s_full + 2;         // [2]
+    uint64_t *ds_ready = dp_full + 2;       // [2]
+    uint64_t *fin = ds_ready + 2;
     uint64_t *drain = fin + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = warp_id(), lane = lane_id();
-    const int bh = blockIdx.x % p.BH;
-    const int qt = p.T - 1 - static_cast<int>(blockIdx.x / p.BH);  // long rows first
+    const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.T, p.head_group);
+    const int bh = ord.head;
+    const int qt = p.T - 1 - ord.rank;  // long rows first
     const int jend = p.causal ? qt + 1 : p.T;
 
     if (threadIdx.x == 0) {
@@ -441,8 +503,11 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(ds_ready, 128);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&dp_full[h], 1);
+            mbar_init(&ds_ready[h], 128);
+        }
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -496,44 +561,82 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             const uint32_t sQ = smem_u32(smem + L::kQOff);
             const uint32_t sdO = smem_u32(smem + L::kdOOff);
-            const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+            const uint32_t tdQ = tmem + 256;
+            auto stage_k = [&](int st) {
+                return smem_u32(smem + L::kStageOff + st * L::kStageBytes);
+            };
+            // S_h = Q K_h^T and dP_h = dO V_h^T, K_h / V_h = key rows [64h, 64h+64)
+            const SDesc dQa = sdesc_make(sQ, 16, 1024), ddOa = sdesc_make(sdO, 16, 1024);
+            const SDesc dK0 = sdesc_make(stage_k(0), 16, 1024);
+            const SDesc dKm0 = sdesc_make(stage_k(0), L::kBoxBytes, 1024);
+            auto issue_sdp = [&](int st, int h) {
+                const uint32_t koff = st * L::kStageBytes + h * 64 * 128;
+                const SDesc bk = sdesc_add(dK0, koff), bv = sdesc_add(dK0, koff + L::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + 64 * h, sdesc_add(dQa, off), sdesc_add(bk, off), kIdescSS,
+                           kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[h]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                    mma_ss(tmem + 128 + 64 * h, sdesc_add(ddOa, off), sdesc_add(bv, off), kIdescSS,
+                           kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&dp_full[h]);
+            };
+            auto next_live = [&](int j) {
+                for (++j; j < jend; ++j)
+                    if (tile_live(p, qt, j)) return j;
+                return jend;
+            };
             bool ok = mbar_wait(q_full, 0, p.ctl, abort_flag);
+            int j = next_live(-1);
             int n = 0;
-            for (int j = 0; ok && j < jend; ++j) {
-                if (!tile_live(p, qt, j)) continue;
+            if (ok && j < jend) {
+                ok = mbar_wait(&full[0], 0, p.ctl, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    issue_sdp(0, 0);
+                    issue_sdp(0, 1);
+                    if (p.ctl.visit_log != nullptr)
+                        p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
+                }
+            }
+            while (ok && j < jend) {
                 const int s = n % L::kStages;
-                if (!mbar_wait(&full[s], (n / L::kStages) & 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sK = smem_u32(smem + L::kStageOff + s * L::kStageBytes);
-                const uint32_t sV = sK + L::kTileBytes;
+                const int s2 = (n + 1) % L::kStages;
+                const int nxt = next_live(j);
+                const SDesc bKm = sdesc_add(dKm0, s * L::kStageBytes);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!mbar_wait(&ds_ready[h], n & 1, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
-                            kIdescSS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)  // dQ += dS_h K_h (K = 64 keys)
+                        mma_ts(tdQ, tmem + 64 * h + kk * 8, sdesc_add(bKm, h * 8192 + kk * 2048),
+                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    if (h == 1) umma_commit(&empty[s]);
+                    if (nxt < jend) {
+                        if (h == 0) {
+                            if (!mbar_wait(&full[s2], ((n + 1) / L::kStages) & 1, p.ctl,
+                                           abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (p.ctl.visit_log != nullptr)
+                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T +
+                                                nxt] |= 4;
+                        }
+                        issue_sdp(s2, h);
+                    }
                 }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tdP, sdesc_sw128(sdO + off, 16, 1024),
-                            sdesc_sw128(sV + off, 16, 1024), kIdescSS, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(s_full);
-                if (p.ctl.visit_log != nullptr)
-                    p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
-                if (!mbar_wait(ds_ready, n & 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)  // dQ += dS K
-                    umma_ts(tdQ, tS + kk * 8, sdesc_sw128(sK + kk * 2048, L::kBoxBytes, 1024),
-                            kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&empty[s]);
+                j = nxt;
                 ++n;
             }
             if (ok && n > 0) umma_commit(fin);
@@ -542,11 +645,12 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
+        const int h = (warp - 2) >> 2;  // key half of every tile this group owns
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int q_row = qt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tdP = tS + 128, tdQ = tS + 256;
+        const uint32_t tS = tmem + lane_base + 64 * h, tdP = tS + 128;
         const float sl2 = p.scale_log2;
         const float lrow = lse_log2(p, bh, q_row);
         const float drow = q_row < p.N ? p.delta[static_cast<size_t>(bh) * p.N + q_row] : 0.f;
@@ -554,37 +658,49 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
         for (int j = 0; j < jend; ++j) {
             if (!tile_live(p, qt, j)) continue;
-            if (!mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
+            if (!mbar_wait_warp(&s_full[h], n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int kv0 = j * kTile;
-            const bool need_mask = (p.causal && j == qt) || (kv0 + kTile > p.N);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tS + 32 * c, a);
-                tmem_ld32(tdP + 32 * c, b);
+            const int kv0 = j * kTile + 64 * h;
+            const bool need_mask = (p.causal && j == qt) || (kv0 + 64 > p.N);
+            float pr[64];  // P of this row's 64 keys, fp32, while the tensor core is on dP
+            {
+                uint32_t a[64];
+                tmem_ld32(tS, a);
+                tmem_ld32(tS + 32, a + 32);
                 tmem_wait_ld();
-                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pa = ex2(fmaf(__uint_as_float(a[2 * e]), sl2, -lrow));
-                    float pb = ex2(fmaf(__uint_as_float(a[2 * e + 1]), sl2, -lrow));
+                for (int e = 0; e < 64; ++e) {
+                    float pv = ex2(fmaf(__uint_as_float(a[e]), sl2, -lrow));
                     if (need_mask) {
-                        const int col = kv0 + 32 * c + 2 * e;
-                        if (col >= p.N || (p.causal && col > q_row)) pa = 0.f;
-                        if (col + 1 >= p.N || (p.causal && col + 1 > q_row)) pb = 0.f;
+                        const int col = kv0 + e;
+                        if (col >= p.N || (p.causal && col > q_row)) pv = 0.f;
                     }
-                    w[e] = pack2<BF16>(pa * (__uint_as_float(b[2 * e]) - drow),
-                                       pb * (__uint_as_float(b[2 * e + 1]) - drow));
+                    pr[e] = pv;
                 }
-                tmem_st16(tS + 16 * c, w);  // over columns already read
+            }
+            if (!mbar_wait_warp(&dp_full[h], n & 1, p.ctl, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                uint32_t b[64];
+                tmem_ld32(tdP, b);
+                tmem_ld32(tdP + 32, b + 32);
+                tmem_wait_ld();
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    w[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(b[2 * e]) - drow),
+                                       pr[2 * e + 1] * (__uint_as_float(b[2 * e + 1]) - drow));
+                tmem_st32(tS, w);  // over columns already read
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(ds_ready);
+            mbar_arrive(&ds_ready[h]);
             ++n;
         }
         if (ok && n > 0) {
@@ -592,14 +708,17 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
         }
         if (ok) {
+            // each group writes half of dQ's columns (times the softmax scale)
             const bool valid = q_row < p.N;
             using T = elem_t<BF16>;
-            T *dq = reinterpret_cast<T *>(p.out0) + (static_cast<size_t>(bh) * p.N + q_row) * D;
+            T *dq = reinterpret_cast<T *>(p.out0) + (static_cast<size_t>(bh) * p.N + q_row) * D +
+                    h * (D / 2);
+            const uint32_t tacc = tmem + lane_base + 256 + h * (D / 2);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t a[32];
                 if (n > 0) {
-                    tmem_ld32(tdQ + 32 * cc, a);
+                    tmem_ld32(tacc + 32 * cc, a);
                     tmem_wait_ld();
                 } else {
 #pragma unroll

@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(320, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
     const int warp = warp_id(), lane = lane_id();
-    const int bh = blockIdx.x % p.BH;
-    const int pair = p.num_pairs - 1 - static_cast<int>(blockIdx.x / p.BH);  // long rows first
+    const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.num_pairs, p.head_group);
+    const int bh = ord.head;
+    const int pair = p.num_pairs - 1 - ord.rank;  // long rows first
     const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
     const bool has1 = qt1 < p.T;
     const int jend = p.causal ? min(has1 ? qt1 : qt0, p.T - 1) + 1 : p.T;
@@ -182,24 +183,27 @@ __global__ void __launch_bounds__(320, 1)
             int prev_vs = 0;
             uint32_t prev_vpar = 0;
 
+            // descriptors of the Q tiles and of slot 0; a slot or k-step only adds an offset
+            const SDesc dq0 = sdesc_make(sQ, 16, 1024);
+            const SDesc dk0 = sdesc_make(sSlots, 16, 1024);                // K: K-major
+            const SDesc dv0 = sdesc_make(sSlots, L::kBoxBytes, 1024);      // V: MN-major
             auto issue_s = [&](int t, int ks) {
-                const uint32_t a0 = sQ + t * L::kTileBytes;
-                const uint32_t b0 = sSlots + ks * L::kTileBytes;
+                const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
+                const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tmem + t * 128, sdesc_sw128(a0 + off, 16, 1024),
-                            sdesc_sw128(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + t * 128, sdesc_add(a, off), sdesc_add(b, off), kIdescS,
+                           kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int vs, bool accumulate) {
-                const uint32_t b0 = sSlots + vs * L::kTileBytes;
+                const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
+                const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk) {
-                    umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                            sdesc_sw128(b0 + kk * 2048, L::kBoxBytes, 1024), kIdescPV,
-                            (accumulate || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 2048),
+                           kIdescPV, kk > 0 ? 1u : acc);
             };
 
             for (int j = 0; ok && j < jend; ++j) {

@@ -12,12 +12,33 @@ namespace fa {
 
 constexpr int kTile = 128;  // query rows / key rows per tile, also the block-mask granularity
 
+// CTA order: heads are taken in groups of `group` so that the tiles streamed by the CTAs that
+// run at the same time (K/V of the forward, Q/dO of dK/dV, K/V of dQ) stay within a slice of
+// L2; inside a group the work unit (query-tile pair or tile) advances slowest, longest first.
+struct CtaOrder {
+    int head;  // b * H + h
+    int rank;  // 0 = the first (longest) work unit of the head
+};
+__host__ __device__ inline CtaOrder cta_order(unsigned cta, int BH, int units, int group) {
+    // 32-bit arithmetic: the grid has fewer than 2^31 CTAs
+    const unsigned per_group = static_cast<unsigned>(group) * static_cast<unsigned>(units);
+    const unsigned g = cta / per_group;
+    const unsigned r = cta - g * per_group;
+    const int left = BH - static_cast<int>(g) * group;
+    const unsigned heads = static_cast<unsigned>(left < group ? left : group);
+    CtaOrder o;
+    o.rank = static_cast<int>(r / heads);
+    o.head = static_cast<int>(g) * group + static_cast<int>(r % heads);
+    return o;
+}
+
 struct FwdParams {
     void *o;                  // [B,H,N,d] output
     float *lse;               // [B,H,N] output
     const uint8_t *mask;      // [T][T] or nullptr
     int BH, N, T;             // heads (B*H), sequence length, tiles per side
     int num_pairs;            // ceil(T / 2): query-tile pairs per head
+    int head_group;           // heads per CTA-order group (see cta_order)
     float scale_log2;         // scale * log2(e)
     int causal;
     Ctl ctl;
@@ -30,6 +51,7 @@ struct BwdParams {
     const float *delta;       // [B,H,N]
     const uint8_t *mask;      // [T][T] or nullptr
     int BH, N, T;
+    int head_group;           // heads per CTA-order group (see cta_order)
     float scale;              // softmax scale (dK and dQ carry it)
     float scale_log2;         // scale * log2(e)
     int causal;

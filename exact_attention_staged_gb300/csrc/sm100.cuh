@@ -168,6 +168,46 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same descriptor as two 32-bit halves, so that the MMA issue loop only adds a k-step's
+// start-address offset (bytes >> 4) to the low word: no 64-bit arithmetic per MMA.  Valid while
+// the start address stays below 256 KB, which every shared-memory address does.
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    SDesc d;
+    d.lo = ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+    d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+    return d;
+}
+__device__ __forceinline__ SDesc sdesc_add(SDesc d, uint32_t byte_offset) {
+    d.lo += byte_offset >> 4;
+    return d;
+}
+
+// D[tmem] (+)= A[smem] * B[smem], descriptors as halves (the issue path of the kernels)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
