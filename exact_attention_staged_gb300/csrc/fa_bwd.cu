@@ -19,8 +19,9 @@
 //   dQ           CTA = one 128-row query tile i.  For every live key tile j:
 //                  S = Q_i K_j^T, dP = dO_i V_j^T, P = exp2(...), dS = P o (dP - D_i),
 //                  dQ += dS K_j (TS MMA), and finally dQ *= scale.
-// In both, two groups of four warps split every 128 x 128 score tile into two 64-wide halves
-// and alternate on the tensor core, the way the forward's two query tiles do.
+// In both, two groups of four warps split every 128 x 128 score tile into two 64-wide column
+// halves, and the MMA warp runs one tile ahead so the groups' exponentials overlap the tensor
+// core (see each kernel's comment for its order).
 #include "fa_internal.h"
 
 #include <cmath>
@@ -75,6 +76,25 @@ __device__ __forceinline__ void store_row32(void *dst, const uint32_t *v, float 
     d[3] = make_uint4(w[12], w[13], w[14], w[15]);
 }
 
+// Store 16 fp32 values (times `mul`) of one row as 16-bit values, 32 bytes.
+template <bool BF16>
+__device__ __forceinline__ void store_row16(void *dst, const uint32_t *v, float mul) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Compute-group geometry shared by both backward kernels: four groups of four warps (one
+// warp per TMEM lane quadrant each), group g owning columns [32g, 32g+32) of every 128-wide
+// score tile.  The CTA also has a load warp and one (dK/dV) or two (dQ) MMA-issuing warps.
+constexpr int kGroups = 4;
+constexpr int kGroupCols = kTile / kGroups;  // 32
+constexpr int kComputeThreads = kGroups * 128;
+
 // ================================================================================ preprocess
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, const void *dout,
@@ -103,74 +123,86 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
 }
 
 // ================================================================================ dK / dV
-// CTA = one 128-row key tile, 320 threads: warp 0 loads, warp 1 issues MMAs, warps 2..5
-// (group 0) and 6..9 (group 1) each own one 64-query half of every 128 x 128 score tile.
-// TMEM: S^T half h at [64h, 64h+64), dP^T half h at [128+64h, ...), dV at [256, 256+d),
-// dK at [256+d, 256+2d).  P^T_h and dS^T_h are packed over the first 32 columns of S^T_h and
-// dP^T_h.  MMA order per query tile n (next tile n+1), for h = 0, 1:
-//   dV += P^T_h dO_h;  dK += dS^T_h Q_h;  S^T_h(n+1);  dP^T_h(n+1)
-// so while one group exponentiates, the tensor core works on the other group's half.
+// CTA = one 128-row key tile, 576 threads: warp 0 loads, warp 1 issues the MMAs, warps 2..17
+// are four compute groups, group g owning query columns [32g, 32g+32) of every score tile.
+// Shared memory: K_j and V_j (stationary), a ring of slots that receives Q_0, dO_0, Q_1, dO_1,
+// ... in that order (each released as soon as its last MMA is done), and a two-entry ring of
+// the tiles' L (logsumexp) and D values, fetched with cp.async so the load warp never stalls.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).  Group g packs its
+// P^T columns into [32g, 32g+16) and its dS^T columns into [128+32g, 128+32g+16).
+// MMA order, one query tile of lookahead: dV(n), S^T(n+1), dK(n), dP^T(n+1), dV(n+1), ...
+// So the exponentials of tile n+1 overlap dK(n) and dP^T(n+1), and dS(n+1) overlaps dV(n+1)
+// and S^T(n+2).  One issuing thread keeps this order exact on the tensor pipe.
 template <int D>
 struct DkvLayout {
     static constexpr int kTileBytes = kTile * D * 2;
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kTile * 128;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kSlots = (D == 128) ? 5 : 10;  // Q / dO ring
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kTileBytes;
-    static constexpr int kStageOff = 2 * kTileBytes;
-    // per stage: Q tile, dO tile, then 128 floats of L*log2e and 128 floats of D
-    static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // kv_full, full[S], empty[S], s_full[2], dp_full[2], p_ready[2], ds_ready[2], final, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 10;
+    static constexpr int kSlotOff = 2 * kTileBytes;
+    static constexpr int kLdOff = kSlotOff + kSlots * kTileBytes;  // 2 x (128 L + 128 D floats)
+    static constexpr int kBarOff = kLdOff + 2 * 1024;
+    // kv_full, full[S], empty[S], ld_full[2], ld_empty[2], s_full, dp_full, p_ready, ds_ready,
+    // final, drain
+    static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kAlloc = kMiscOff + 16 + 1024;
-    static constexpr int kThreads = 320;
+    static constexpr int kAlloc = kMiscOff + 16;  // the dynamic base is 1024-aligned (checked)
+    static constexpr int kThreads = 64 + kComputeThreads;
+    static constexpr int kComputeWarp0 = 2;
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(64 + kComputeThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
     using L = DkvLayout<D>;
-    constexpr uint32_t kIdescSS = idesc_f16(128, 64, BF16, false);  // S^T_h, dP^T_h
-    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);    // dV, dK
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);  // S^T, dP^T
+    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dV, dK
+    extern __shared__ uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // layouts assume a 1024-aligned base; never observed
+        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrTimeout);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *kv_full = bars;
     uint64_t *full = bars + 1;
-    uint64_t *empty = full + L::kStages;
-    uint64_t *s_full = empty + L::kStages;  // [2]
-    uint64_t *dp_full = s_full + 2;         // [2]
-    uint64_t *p_ready = dp_full + 2;        // [2]
-    uint64_t *ds_ready = p_ready + 2;       // [2]
-    uint64_t *fin = ds_ready + 2;
+    uint64_t *empty = full + L::kSlots;
+    uint64_t *ld_full = empty + L::kSlots;  // [2]
+    uint64_t *ld_empty = ld_full + 2;       // [2]
+    uint64_t *s_full = ld_empty + 2;
+    uint64_t *dp_full = s_full + 1;
+    uint64_t *p_ready = dp_full + 1;
+    uint64_t *ds_ready = p_ready + 1;
+    uint64_t *fin = ds_ready + 1;
     uint64_t *drain = fin + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+    float *ld_ring = reinterpret_cast<float *>(smem + L::kLdOff);
 
     const int warp = warp_id(), lane = lane_id();
     const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.T, p.head_group);
     const int bh = ord.head;
-    const int kt = ord.rank;              // key tile; tile 0 sees the most query tiles when causal
-    const int i0 = p.causal ? kt : 0;     // first query tile that can see it
+    const int kt = ord.rank;           // key tile; tile 0 sees the most query tiles when causal
+    const int i0 = p.causal ? kt : 0;  // first query tile that can see it
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int s = 0; s < L::kStages; ++s) {
-            mbar_init(&full[s], 2);  // TMA bytes + the producer warp's L/D stores
+        for (int s = 0; s < L::kSlots; ++s) {
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(&s_full[h], 1);
-            mbar_init(&dp_full[h], 1);
-            mbar_init(&p_ready[h], 128);
-            mbar_init(&ds_ready[h], 128);
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(&ld_full[e], 32);   // one cp.async completion per lane of the load warp
+            mbar_init(&ld_empty[e], kComputeThreads);  // every compute thread, after its dS
         }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, kComputeThreads);
+        mbar_init(ds_ready, kComputeThreads);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -186,7 +218,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- producer warp
+        // ---------------------------------------------------------------- load warp
         if (lane == 0) {
             mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes);
             for (int b = 0; b < L::kBoxes; ++b) {
@@ -196,137 +228,140 @@ __global__ void __launch_bounds__(320, 1)
                             kv_full);
             }
         }
-        int n = 0;
+        int n = 0;  // query tiles issued
         bool ok = true;
         for (int i = i0; i < p.T && ok; ++i) {
             if (!tile_live(p, i, kt)) continue;
-            const int s = n % L::kStages;
-            const uint32_t par = ((n / L::kStages) & 1) ^ 1;
+            for (int x = 0; x < 2 && ok; ++x) {  // Q_i then dO_i
+                const int l = 2 * n + x;
+                const int s = l % L::kSlots;
+                int got = 0;
+                if (lane == 0) {
+                    got = mbar_wait(&empty[s], ((l / L::kSlots) & 1) ^ 1, p.ctl, abort_flag);
+                    if (got) {
+                        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+                        uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
+                        for (int b = 0; b < L::kBoxes; ++b)
+                            tma_load_3d(dst + b * L::kBoxBytes, x ? &tmdo : &tmq, b * 64,
+                                        i * kTile, bh, &full[s]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+            }
+            if (!ok) break;
+            // L and D of tile i into ring entry n % 2, once tile n - 2 has released it
+            const int e = n & 1;
             int got = 0;
-            if (lane == 0) got = mbar_wait(&empty[s], par, p.ctl, abort_flag) ? 1 : 0;
-            got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) {
+            if (lane == 0) got = mbar_wait(&ld_empty[e], ((n >> 1) & 1) ^ 1, p.ctl, abort_flag);
+            if (!__shfl_sync(0xffffffffu, got, 0)) {
                 ok = false;
                 break;
             }
-            uint8_t *st = smem + L::kStageOff + s * L::kStageBytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], 2 * L::kTileBytes);
-                for (int b = 0; b < L::kBoxes; ++b) {
-                    tma_load_3d(st + b * L::kBoxBytes, &tmq, b * 64, i * kTile, bh, &full[s]);
-                    tma_load_3d(st + L::kTileBytes + b * L::kBoxBytes, &tmdo, b * 64, i * kTile,
-                                bh, &full[s]);
-                }
-            }
-            float *sl = reinterpret_cast<float *>(st + 2 * L::kTileBytes);
-            float *sd = sl + 128;
+            float *dl = ld_ring + e * 256;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = lane + 32 * e;
+            for (int k = 0; k < 4; ++k) {
+                const int c = lane + 32 * k;
                 const int row = i * kTile + c;
-                sl[c] = lse_log2(p, bh, row);
-                sd[c] = row < p.N ? p.delta[static_cast<size_t>(bh) * p.N + row] : 0.f;
+                const bool in = row < p.N;
+                const size_t off = static_cast<size_t>(bh) * p.N + (in ? row : 0);
+                cp_async_4(dl + c, p.lse + off, in);
+                cp_async_4(dl + 128 + c, p.delta + off, in);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
+            cp_async_arrive_noinc(&ld_full[e]);
             ++n;
         }
         if (lane == 0 && (!ok || *abort_flag)) {
             drain_wait(kv_full, 0, p.ctl);
-            const int first = n > L::kStages ? n - L::kStages : 0;
-            for (int l = first; l < n; ++l)
-                drain_wait(&full[l % L::kStages], (l / L::kStages) & 1, p.ctl);
+            const int issued = 2 * n;
+            const int first = issued > L::kSlots ? issued - L::kSlots : 0;
+            for (int l = first; l < issued; ++l)
+                drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
         }
+        cp_async_wait_all();
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t sK = smem_u32(smem + L::kKOff);
-            const uint32_t sV = smem_u32(smem + L::kVOff);
-            const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
-            auto stage_q = [&](int st) {
-                return smem_u32(smem + L::kStageOff + st * L::kStageBytes);
+            const uint32_t sSlot = smem_u32(smem + L::kSlotOff);
+            const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+            const SDesc dK0 = sdesc_make(smem_u32(smem + L::kKOff), 16, 1024);
+            const SDesc dV0 = sdesc_make(smem_u32(smem + L::kVOff), 16, 1024);
+            const SDesc dSk = sdesc_make(sSlot, 16, 1024);            // slot as K-major B
+            const SDesc dSm = sdesc_make(sSlot, L::kBoxBytes, 1024);  // slot as MN-major B
+            auto slot_of = [&](int l) { return l % L::kSlots; };
+            auto full_wait = [&](int l) {
+                return mbar_wait(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
             };
-            // S^T_h = K Q_h^T and dP^T_h = V dO_h^T, Q_h / dO_h = query rows [64h, 64h+64)
-            const SDesc dK0 = sdesc_make(sK, 16, 1024), dV0 = sdesc_make(sV, 16, 1024);
-            const SDesc dQk0 = sdesc_make(stage_q(0), 16, 1024);
-            const SDesc dQm0 = sdesc_make(stage_q(0), L::kBoxBytes, 1024);
-            auto issue_sdp = [&](int st, int h) {
-                const uint32_t qoff = st * L::kStageBytes + h * 64 * 128;
-                const SDesc bq = sdesc_add(dQk0, qoff), bdo = sdesc_add(dQk0, qoff + L::kTileBytes);
+            auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d, A stationary
+                const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + 64 * h, sdesc_add(dK0, off), sdesc_add(bq, off), kIdescSS,
-                           kk > 0 ? 1u : 0u);
+                    mma_ss(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&s_full[h]);
+            };
+            auto issue_ts = [&](uint32_t d, uint32_t a_col, int l, bool acc) {  // K = 128 queries
+                const SDesc b = sdesc_add(dSm, slot_of(l) * L::kTileBytes);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + 128 + 64 * h, sdesc_add(dV0, off), sdesc_add(bdo, off), kIdescSS,
-                           kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&dp_full[h]);
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                    mma_ts(d, a_col + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(b, kk * 2048),
+                           kIdescTS, (acc || kk > 0) ? 1u : 0u);
             };
             auto next_live = [&](int i) {
                 for (++i; i < p.T; ++i)
                     if (tile_live(p, i, kt)) return i;
                 return p.T;
             };
+            auto log_visit = [&](int i) {
+                if (p.ctl.visit_log != nullptr)
+                    p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + i) * p.T + kt] |= 2;
+            };
             bool ok = mbar_wait(kv_full, 0, p.ctl, abort_flag);
             int i = next_live(i0 - 1);
             int n = 0;
             if (ok && i < p.T) {
-                ok = mbar_wait(&full[0], 0, p.ctl, abort_flag);
+                ok = full_wait(0) && full_wait(1);
                 if (ok) {
-                    tc_fence_after();
-                    issue_sdp(0, 0);
-                    issue_sdp(0, 1);
-                    if (p.ctl.visit_log != nullptr)
-                        p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + i) * p.T + kt] |= 2;
+                    issue_ss(tS, dK0, 0);
+                    umma_commit(s_full);
+                    issue_ss(tdP, dV0, 1);
+                    umma_commit(dp_full);
+                    log_visit(i);
                 }
             }
             while (ok && i < p.T) {
-                const int s = n % L::kStages;
-                const int s2 = (n + 1) % L::kStages;
                 const int nxt = next_live(i);
-                const SDesc bQm = sdesc_add(dQm0, s * L::kStageBytes);
-                const SDesc bdOm = sdesc_add(bQm, L::kTileBytes);
-                for (int h = 0; h < 2 && ok; ++h) {
-                    if (!mbar_wait(&p_ready[h], n & 1, p.ctl, abort_flag)) {
+                const int lq = 2 * n, ldo = 2 * n + 1;  // this tile's Q and dO loads
+                if (!mbar_wait(p_ready, n & 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_ts(tdV, tS, ldo, n > 0);  // dV += P^T dO
+                umma_commit(&empty[slot_of(ldo)]);
+                if (nxt < p.T) {
+                    if (!full_wait(lq + 2)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // dV += P^T_h dO_h (K = 64 queries)
-                        mma_ts(tdV, tmem + 64 * h + kk * 8, sdesc_add(bdOm, h * 8192 + kk * 2048),
-                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (!mbar_wait(&ds_ready[h], n & 1, p.ctl, abort_flag)) {
+                    issue_ss(tS, dK0, lq + 2);  // S^T(n+1) = K Q^T
+                    umma_commit(s_full);
+                    log_visit(nxt);
+                }
+                if (!mbar_wait(ds_ready, n & 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_ts(tdK, tdP, lq, n > 0);  // dK += dS^T Q
+                umma_commit(&empty[slot_of(lq)]);
+                if (nxt < p.T) {
+                    if (!full_wait(ldo + 2)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_h Q_h
-                        mma_ts(tdK, tmem + 128 + 64 * h + kk * 8, sdesc_add(bQm, h * 8192 + kk * 2048),
-                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (h == 1) umma_commit(&empty[s]);
-                    if (nxt < p.T) {
-                        if (h == 0) {
-                            if (!mbar_wait(&full[s2], ((n + 1) / L::kStages) & 1, p.ctl,
-                                           abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            if (p.ctl.visit_log != nullptr)
-                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + nxt) * p.T +
-                                                kt] |= 2;
-                        }
-                        issue_sdp(s2, h);
-                    }
+                    issue_ss(tdP, dV0, ldo + 2);  // dP^T(n+1) = V dO^T
+                    umma_commit(dp_full);
                 }
                 i = nxt;
                 ++n;
@@ -338,76 +373,82 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- compute groups
-        const int h = (warp - 2) >> 2;    // query half of every tile this group owns
+        const int g = (warp - L::kComputeWarp0) >> 2;  // query columns [32g, 32g+32)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // key row within the tile
         const int k_row = kt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + 64 * h, tdP = tS + 128;
+        const uint32_t tS = tmem + lane_base + kGroupCols * g, tdP = tS + 128;
         const float sl2 = p.scale_log2;
         int n = 0;
         bool ok = true;
         for (int i = i0; i < p.T; ++i) {
             if (!tile_live(p, i, kt)) continue;
-            const int s = n % L::kStages;
-            // the stage's L and D values were stored by the producer warp before its arrive
-            if (!mbar_wait_warp(&full[s], (n / L::kStages) & 1, p.ctl, abort_flag) ||
-                !mbar_wait_warp(&s_full[h], n & 1, p.ctl, abort_flag)) {
+            const int e = n & 1;
+            if (!mbar_wait_warp(&ld_full[e], (n >> 1) & 1, p.ctl, abort_flag) ||
+                !mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float *sl =
-                reinterpret_cast<const float *>(smem + L::kStageOff + s * L::kStageBytes +
-                                                2 * L::kTileBytes) + 64 * h;
-            const float *sd = sl + 128;
-            // query q sees key k only when k <= q: only the diagonal tile needs the compare
-            const bool diag = p.causal && i == kt;
-            uint32_t pk[32];  // P^T of this row's 64 queries, packed 16-bit pairs
+            const float4 *lv = reinterpret_cast<const float4 *>(ld_ring + e * 256 + kGroupCols * g);
+            const float4 *dv = lv + 32;  // D values 128 floats after L
+            // query q sees key k only when k <= q (causal) and q < N
+            const int q_base = i * kTile + kGroupCols * g;
+            const bool need_mask = (p.causal && i == kt) || (q_base + kGroupCols > p.N);
+            uint32_t pk[16];  // P^T of this row's 32 queries, packed 16-bit pairs
             {
-                uint32_t r[64];
+                uint32_t r[32];
                 tmem_ld32(tS, r);
-                tmem_ld32(tS + 32, r + 32);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int q0 = 2 * e;
-                    float a = ex2(fmaf(__uint_as_float(r[q0]), sl2, -sl[q0]));
-                    float b = ex2(fmaf(__uint_as_float(r[q0 + 1]), sl2, -sl[q0 + 1]));
-                    if (diag) {
-                        if (64 * h + q0 < row) a = 0.f;
-                        if (64 * h + q0 + 1 < row) b = 0.f;
+                for (int c = 0; c < 8; ++c) {
+                    const float4 lq = lv[c];
+                    float pv[4] = {ex2(fmaf(__uint_as_float(r[4 * c]), sl2, -lq.x * kLog2e)),
+                                   ex2(fmaf(__uint_as_float(r[4 * c + 1]), sl2, -lq.y * kLog2e)),
+                                   ex2(fmaf(__uint_as_float(r[4 * c + 2]), sl2, -lq.z * kLog2e)),
+                                   ex2(fmaf(__uint_as_float(r[4 * c + 3]), sl2, -lq.w * kLog2e))};
+                    if (need_mask) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int q = q_base + 4 * c + u;
+                            if (q >= p.N || (p.causal && q < k_row)) pv[u] = 0.f;
+                        }
                     }
-                    pk[e] = pack2<BF16>(a, b);
+                    pk[2 * c] = pack2<BF16>(pv[0], pv[1]);
+                    pk[2 * c + 1] = pack2<BF16>(pv[2], pv[3]);
                 }
             }
-            tmem_st32(tS, pk);
+            tmem_st16(tS, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_ready[h]);
-            if (!mbar_wait_warp(&dp_full[h], n & 1, p.ctl, abort_flag)) {
+            mbar_arrive(p_ready);
+            if (!mbar_wait_warp(dp_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             {
-                uint32_t r[64];
+                uint32_t r[32];
                 tmem_ld32(tdP, r);
-                tmem_ld32(tdP + 32, r + 32);
                 tmem_wait_ld();
-                uint32_t w[32];
+                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int q0 = 2 * e;
-                    const float2 pp = unpack2<BF16>(pk[e]);
-                    w[e] = pack2<BF16>(pp.x * (__uint_as_float(r[q0]) - sd[q0]),
-                                       pp.y * (__uint_as_float(r[q0 + 1]) - sd[q0 + 1]));
+                for (int c = 0; c < 8; ++c) {
+                    const float4 dq = dv[c];
+                    const float2 p0 = unpack2<BF16>(pk[2 * c]);
+                    const float2 p1 = unpack2<BF16>(pk[2 * c + 1]);
+                    w[2 * c] = pack2<BF16>(p0.x * (__uint_as_float(r[4 * c]) - dq.x),
+                                           p0.y * (__uint_as_float(r[4 * c + 1]) - dq.y));
+                    w[2 * c + 1] = pack2<BF16>(p1.x * (__uint_as_float(r[4 * c + 2]) - dq.z),
+                                               p1.y * (__uint_as_float(r[4 * c + 3]) - dq.w));
                 }
-                tmem_st32(tdP, w);  // over columns already read
+                tmem_st16(tdP, w);  // over columns already read
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&ds_ready[h]);
+            mbar_arrive(ds_ready);
+            mbar_arrive(&ld_empty[e]);
             ++n;
         }
         if (ok && n > 0) {
@@ -415,22 +456,23 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
         }
         if (ok) {
-            // group 0 writes dV, group 1 writes dK (times the softmax scale)
+            // groups 0, 1 write the two column halves of dV; groups 2, 3 those of dK (x scale)
             const bool valid = k_row < p.N;
             using T = elem_t<BF16>;
-            T *dst = reinterpret_cast<T *>(h == 0 ? p.out1 : p.out0) +
-                     (static_cast<size_t>(bh) * p.N + k_row) * D;
-            const uint32_t tacc = tmem + lane_base + 256 + h * D;
-            const float mul = h == 0 ? 1.f : p.scale;
+            const int half = g & 1;
+            T *dst = reinterpret_cast<T *>(g < 2 ? p.out1 : p.out0) +
+                     (static_cast<size_t>(bh) * p.N + k_row) * D + half * (D / 2);
+            const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
+            const float mul = g < 2 ? 1.f : p.scale;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t a[32];
                 if (n > 0) {
                     tmem_ld32(tacc + 32 * cc, a);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    for (int e2 = 0; e2 < 32; ++e2) a[e2] = 0u;
                 }
                 if (valid) store_row32<BF16>(dst + 32 * cc, a, mul);
             }
@@ -446,48 +488,57 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ================================================================================ dQ
-// CTA = one 128-row query tile, 320 threads: warp 0 loads, warp 1 issues MMAs, warps 2..5
-// (group 0) and 6..9 (group 1) each own one 64-key half of every 128 x 128 score tile.
-// TMEM: S half h at [64h, 64h+64), dP half h at [128+64h, ...), dQ at [256, 256+d); dS_h is
-// packed over the first 32 columns of S_h.  MMA order per key tile n (next n+1), h = 0, 1:
-//   dQ += dS_h K_h;  S_h(n+1);  dP_h(n+1)
+// CTA = one 128-row query tile, 608 threads: warp 0 loads, warp 1 issues S and dQ, warp 2
+// issues dP, warps 3..18 are four compute groups, group g owning key columns [32g, 32g+32) of
+// every score tile.  Two issuers: the MMA pipe holds only about two MMAs, and the two chains
+// (S and dQ; dP) need no order between them, so one thread's waits no longer idle the pipe.
+// Shared memory: Q_i and dO_i (stationary) and a ring of slots receiving K_0, V_0, K_1, V_1, ...
+// TMEM: two S buffers [0,128) and [128,256) (tile n uses buffer n % 2), dP [256,384),
+// dQ [384,384+d).  Group g packs its dS columns into the first 16 columns of its S quarter.
+// MMA order: warp 1 runs dQ(n), S(n+2), dQ(n+1), ...; warp 2 runs dP(n+1), dP(n+2), ... once
+// the groups are done with dP(n).  The next tile's S is already in TMEM while the groups work on
+// tile n+1, and S(n+2) overwrites buffer n % 2 only after dQ(n) has read it.  Each S buffer has
+// its own dS-ready barrier, so neither issuer can fall two phases behind one.
 template <int D>
 struct DqLayout {
     static constexpr int kTileBytes = kTile * D * 2;
     static constexpr int kBoxes = D / 64;
     static constexpr int kBoxBytes = kTile * 128;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kSlots = (D == 128) ? 5 : 10;  // K / V ring
     static constexpr int kQOff = 0;
     static constexpr int kdOOff = kTileBytes;
-    static constexpr int kStageOff = 2 * kTileBytes;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile, V tile
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-    // q_full, full[S], empty[S], s_full[2], dp_full[2], ds_ready[2], final, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 8;
+    static constexpr int kSlotOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+    // q_full, full[S], empty[S], s_full[2], dp_full, ds_ready[2], final, drain[2]
+    static constexpr int kNumBars = 1 + 2 * kSlots + 8;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kAlloc = kMiscOff + 16 + 1024;
-    static constexpr int kThreads = 320;
+    static constexpr int kAlloc = kMiscOff + 16;  // the dynamic base is 1024-aligned (checked)
+    static constexpr int kThreads = 96 + kComputeThreads;
+    static constexpr int kComputeWarp0 = 3;
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(96 + kComputeThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
     using L = DqLayout<D>;
-    constexpr uint32_t kIdescSS = idesc_f16(128, 64, BF16, false);  // S_h, dP_h
-    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);    // dQ
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);  // S, dP
+    constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dQ
+    extern __shared__ uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // layouts assume a 1024-aligned base; never observed
+        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrTimeout);
+        return;
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *full = bars + 1;
-    uint64_t *empty = full + L::kStages;
-    uint64_t *s_full = empty + L::kStages;  // [2]
-    uint64_t *dp_full = s_full + 2;         // [2]
-    uint64_t *ds_ready = dp_full + 2;       // [2]
+    uint64_t *empty = full + L::kSlots;
+    uint64_t *s_full = empty + L::kSlots;  // [2]
+    uint64_t *dp_full = s_full + 2;
+    uint64_t *ds_ready = dp_full + 1;       // [2], one per S buffer
     uint64_t *fin = ds_ready + 2;
-    uint64_t *drain = fin + 1;
+    uint64_t *drain = fin + 1;              // [2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -499,17 +550,18 @@ __global__ void __launch_bounds__(320, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < L::kStages; ++s) {
+        for (int s = 0; s < L::kSlots; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int h = 0; h < 2; ++h) {
-            mbar_init(&s_full[h], 1);
-            mbar_init(&dp_full[h], 1);
-            mbar_init(&ds_ready[h], 128);
-        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(dp_full, 1);
+        mbar_init(&ds_ready[0], kComputeThreads);
+        mbar_init(&ds_ready[1], kComputeThreads);
         mbar_init(fin, 1);
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -531,126 +583,160 @@ __global__ void __launch_bounds__(320, 1)
                 tma_load_3d(smem + L::kdOOff + b * L::kBoxBytes, &tmdo, b * 64, qt * kTile, bh,
                             q_full);
             }
-            int n = 0;
+            int l = 0;  // loads issued: K_n is load 2n, V_n load 2n + 1
             bool ok = true;
             for (int j = 0; j < jend && ok; ++j) {
                 if (!tile_live(p, qt, j)) continue;
-                const int s = n % L::kStages;
-                if (!mbar_wait(&empty[s], ((n / L::kStages) & 1) ^ 1, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
+                for (int x = 0; x < 2; ++x, ++l) {
+                    const int s = l % L::kSlots;
+                    if (!mbar_wait(&empty[s], ((l / L::kSlots) & 1) ^ 1, p.ctl, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+                    uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(dst + b * L::kBoxBytes, x ? &tmv : &tmk, b * 64, j * kTile,
+                                    bh, &full[s]);
                 }
-                uint8_t *st = smem + L::kStageOff + s * L::kStageBytes;
-                mbar_arrive_expect_tx(&full[s], 2 * L::kTileBytes);
-                for (int b = 0; b < L::kBoxes; ++b) {
-                    tma_load_3d(st + b * L::kBoxBytes, &tmk, b * 64, j * kTile, bh, &full[s]);
-                    tma_load_3d(st + L::kTileBytes + b * L::kBoxBytes, &tmv, b * 64, j * kTile,
-                                bh, &full[s]);
-                }
-                ++n;
             }
             if (!ok || *abort_flag) {
                 drain_wait(q_full, 0, p.ctl);
-                const int first = n > L::kStages ? n - L::kStages : 0;
-                for (int l = first; l < n; ++l)
-                    drain_wait(&full[l % L::kStages], (l / L::kStages) & 1, p.ctl);
+                const int first = l > L::kSlots ? l - L::kSlots : 0;
+                for (int m = first; m < l; ++m)
+                    drain_wait(&full[m % L::kSlots], (m / L::kSlots) & 1, p.ctl);
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp <= 2) {
         if (lane == 0) {
-            const uint32_t sQ = smem_u32(smem + L::kQOff);
-            const uint32_t sdO = smem_u32(smem + L::kdOOff);
-            const uint32_t tdQ = tmem + 256;
-            auto stage_k = [&](int st) {
-                return smem_u32(smem + L::kStageOff + st * L::kStageBytes);
+            const bool sq = warp == 1;  // warp 1: S and dQ; warp 2: dP
+            const uint32_t sSlot = smem_u32(smem + L::kSlotOff);
+            const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+            const SDesc dQa = sdesc_make(smem_u32(smem + L::kQOff), 16, 1024);
+            const SDesc ddOa = sdesc_make(smem_u32(smem + L::kdOOff), 16, 1024);
+            const SDesc dSk = sdesc_make(sSlot, 16, 1024);            // slot as K-major B
+            const SDesc dSm = sdesc_make(sSlot, L::kBoxBytes, 1024);  // slot as MN-major B
+            auto slot_of = [&](int l) { return l % L::kSlots; };
+            auto full_wait = [&](int l) {
+                return mbar_wait(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
             };
-            // S_h = Q K_h^T and dP_h = dO V_h^T, K_h / V_h = key rows [64h, 64h+64)
-            const SDesc dQa = sdesc_make(sQ, 16, 1024), ddOa = sdesc_make(sdO, 16, 1024);
-            const SDesc dK0 = sdesc_make(stage_k(0), 16, 1024);
-            const SDesc dKm0 = sdesc_make(stage_k(0), L::kBoxBytes, 1024);
-            auto issue_sdp = [&](int st, int h) {
-                const uint32_t koff = st * L::kStageBytes + h * 64 * 128;
-                const SDesc bk = sdesc_add(dK0, koff), bv = sdesc_add(dK0, koff + L::kTileBytes);
+            auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d
+                const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + 64 * h, sdesc_add(dQa, off), sdesc_add(bk, off), kIdescSS,
-                           kk > 0 ? 1u : 0u);
+                    mma_ss(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&s_full[h]);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + 128 + 64 * h, sdesc_add(ddOa, off), sdesc_add(bv, off), kIdescSS,
-                           kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&dp_full[h]);
             };
             auto next_live = [&](int j) {
                 for (++j; j < jend; ++j)
                     if (tile_live(p, qt, j)) return j;
                 return jend;
             };
+            auto ds_wait = [&](int n) {
+                return mbar_wait(&ds_ready[n & 1], (n >> 1) & 1, p.ctl, abort_flag);
+            };
             bool ok = mbar_wait(q_full, 0, p.ctl, abort_flag);
             int j = next_live(-1);
+            int j1 = j < jend ? next_live(j) : jend;  // tile n + 1
             int n = 0;
-            if (ok && j < jend) {
-                ok = mbar_wait(&full[0], 0, p.ctl, abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    issue_sdp(0, 0);
-                    issue_sdp(0, 1);
-                    if (p.ctl.visit_log != nullptr)
-                        p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
+            if (sq) {
+                // S(0) -> buffer 0, S(1) -> buffer 1; then per tile: dQ(n), S(n+2)
+                if (ok && j < jend) {
+                    ok = full_wait(0);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_ss(tmem, dQa, 0);
+                        umma_commit(&s_full[0]);
+                        if (p.ctl.visit_log != nullptr)
+                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
+                    }
+                    if (ok && j1 < jend) {
+                        ok = full_wait(2);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_ss(tmem + 128, dQa, 2);
+                            umma_commit(&s_full[1]);
+                            if (p.ctl.visit_log != nullptr)
+                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j1] |= 4;
+                        }
+                    }
                 }
-            }
-            while (ok && j < jend) {
-                const int s = n % L::kStages;
-                const int s2 = (n + 1) % L::kStages;
-                const int nxt = next_live(j);
-                const SDesc bKm = sdesc_add(dKm0, s * L::kStageBytes);
-                for (int h = 0; h < 2 && ok; ++h) {
-                    if (!mbar_wait(&ds_ready[h], n & 1, p.ctl, abort_flag)) {
+                while (ok && j < jend) {
+                    const int j2 = j1 < jend ? next_live(j1) : jend;  // tile n + 2
+                    const uint32_t buf = tmem + 128 * (n & 1);
+                    if (!ds_wait(n)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    {  // dQ += dS K_n, K = 128 keys
+                        const SDesc b = sdesc_add(dSm, slot_of(2 * n) * L::kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // dQ += dS_h K_h (K = 64 keys)
-                        mma_ts(tdQ, tmem + 64 * h + kk * 8, sdesc_add(bKm, h * 8192 + kk * 2048),
-                               kIdescTS, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    if (h == 1) umma_commit(&empty[s]);
-                    if (nxt < jend) {
-                        if (h == 0) {
-                            if (!mbar_wait(&full[s2], ((n + 1) / L::kStages) & 1, p.ctl,
-                                           abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            if (p.ctl.visit_log != nullptr)
-                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T +
-                                                nxt] |= 4;
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ts(tdQ, buf + 32 * (kk >> 1) + 8 * (kk & 1),
+                                   sdesc_add(b, kk * 2048), kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(&empty[slot_of(2 * n)]);
+                    }
+                    if (j2 < jend) {  // S(n+2) into this buffer, after dQ(n) read it
+                        if (!full_wait(2 * n + 4)) {
+                            ok = false;
+                            break;
                         }
-                        issue_sdp(s2, h);
+                        tc_fence_after();
+                        issue_ss(buf, dQa, 2 * n + 4);
+                        umma_commit(&s_full[n & 1]);
+                        if (p.ctl.visit_log != nullptr)
+                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j2] |= 4;
+                    }
+                    j = j1;
+                    j1 = j2;
+                    ++n;
+                }
+                if (ok && n > 0) umma_commit(fin);
+            } else {
+                // dP(0); then per tile: once the groups are done with dP(n), dP(n+1)
+                if (ok && j < jend) {
+                    ok = full_wait(1);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_ss(tdP, ddOa, 1);
+                        umma_commit(dp_full);
+                        umma_commit(&empty[slot_of(1)]);
                     }
                 }
-                j = nxt;
-                ++n;
+                while (ok && j < jend) {
+                    if (!ds_wait(n)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j1 < jend) {
+                        if (!full_wait(2 * n + 3)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_ss(tdP, ddOa, 2 * n + 3);
+                        umma_commit(dp_full);
+                        umma_commit(&empty[slot_of(2 * n + 3)]);
+                    }
+                    j = j1;
+                    j1 = j1 < jend ? next_live(j1) : jend;
+                    ++n;
+                }
             }
-            if (ok && n > 0) umma_commit(fin);
-            umma_commit(drain);
-            drain_wait(drain, 0, p.ctl);
+            umma_commit(&drain[sq ? 0 : 1]);
+            drain_wait(&drain[sq ? 0 : 1], 0, p.ctl);
         }
         __syncwarp();
     } else {
-        const int h = (warp - 2) >> 2;  // key half of every tile this group owns
+        const int g = (warp - L::kComputeWarp0) >> 2;  // key columns [32g, 32g+32)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int q_row = qt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + 64 * h, tdP = tS + 128;
+        const uint32_t tdP = tmem + lane_base + 256 + kGroupCols * g;
         const float sl2 = p.scale_log2;
         const float lrow = lse_log2(p, bh, q_row);
         const float drow = q_row < p.N ? p.delta[static_cast<size_t>(bh) * p.N + q_row] : 0.f;
@@ -658,21 +744,22 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int j = 0; j < jend; ++j) {
             if (!tile_live(p, qt, j)) continue;
-            if (!mbar_wait_warp(&s_full[h], n & 1, p.ctl, abort_flag)) {
+            const int b = n & 1;
+            const uint32_t tS = tmem + lane_base + 128 * b + kGroupCols * g;
+            if (!mbar_wait_warp(&s_full[b], (n >> 1) & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int kv0 = j * kTile + 64 * h;
-            const bool need_mask = (p.causal && j == qt) || (kv0 + 64 > p.N);
-            float pr[64];  // P of this row's 64 keys, fp32, while the tensor core is on dP
+            const int kv0 = j * kTile + kGroupCols * g;
+            const bool need_mask = (p.causal && j == qt) || (kv0 + kGroupCols > p.N);
+            float pr[32];  // P of this row's 32 keys, while the tensor core is on dP
             {
-                uint32_t a[64];
+                uint32_t a[32];
                 tmem_ld32(tS, a);
-                tmem_ld32(tS + 32, a + 32);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
+                for (int e = 0; e < 32; ++e) {
                     float pv = ex2(fmaf(__uint_as_float(a[e]), sl2, -lrow));
                     if (need_mask) {
                         const int col = kv0 + e;
@@ -681,26 +768,25 @@ __global__ void __launch_bounds__(320, 1)
                     pr[e] = pv;
                 }
             }
-            if (!mbar_wait_warp(&dp_full[h], n & 1, p.ctl, abort_flag)) {
+            if (!mbar_wait_warp(dp_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             {
-                uint32_t b[64];
-                tmem_ld32(tdP, b);
-                tmem_ld32(tdP + 32, b + 32);
+                uint32_t bv[32];
+                tmem_ld32(tdP, bv);
                 tmem_wait_ld();
-                uint32_t w[32];
+                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    w[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(b[2 * e]) - drow),
-                                       pr[2 * e + 1] * (__uint_as_float(b[2 * e + 1]) - drow));
-                tmem_st32(tS, w);  // over columns already read
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(bv[2 * e]) - drow),
+                                       pr[2 * e + 1] * (__uint_as_float(bv[2 * e + 1]) - drow));
+                tmem_st16(tS, w);  // over columns already read
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&ds_ready[h]);
+            mbar_arrive(&ds_ready[b]);
             ++n;
         }
         if (ok && n > 0) {
@@ -708,23 +794,23 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
         }
         if (ok) {
-            // each group writes half of dQ's columns (times the softmax scale)
+            // group g writes dQ columns [g*d/4, (g+1)*d/4) (times the softmax scale)
             const bool valid = q_row < p.N;
             using T = elem_t<BF16>;
             T *dq = reinterpret_cast<T *>(p.out0) + (static_cast<size_t>(bh) * p.N + q_row) * D +
-                    h * (D / 2);
-            const uint32_t tacc = tmem + lane_base + 256 + h * (D / 2);
+                    g * (D / 4);
+            const uint32_t tacc = tmem + lane_base + 384 + g * (D / 4);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t a[32];
+                uint32_t a[16];
                 if (n > 0) {
-                    tmem_ld32(tacc + 32 * cc, a);
+                    tmem_ld16(tacc + 16 * cc, a);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = 0u;
+                    for (int e = 0; e < 16; ++e) a[e] = 0u;
                 }
-                if (valid) store_row32<BF16>(dq + 32 * cc, a, p.scale);
+                if (valid) store_row16<BF16>(dq + 16 * cc, a, p.scale);
             }
         }
     }

@@ -79,6 +79,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the hardware parks the waiting thread until the phase
+// completes or the hint (ns) runs out, so a waiting warp does not spin through issue slots that
+// the warp sharing its scheduler needs.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (and records a timeout in
 // the status word and in the CTA's abort flag) when the bound runs out, or when another warp
 // of the CTA has already given up.  Never traps.
@@ -87,15 +103,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > ctl.wait_limit_ns) {
-                *abort_flag = 1;
-                atomicExch(ctl.status, kErrTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > ctl.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicExch(ctl.status, kErrTimeout);
+            return false;
         }
     }
 }
@@ -122,6 +136,23 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// cp.async: 4-byte copies global -> shared (zero-filled when `valid` is false), with completion
+// reported to an mbarrier so the issuing warp never waits on the global load.
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gsrc, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+// Arrive on `bar` (without raising its expected count) once this thread's cp.async are done.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------------
@@ -255,6 +286,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -284,6 +325,18 @@ __device__ __forceinline__ void tmem_wait_ld() {
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Register rebalancing between warpgroups (all four warps of a warpgroup execute it): the
+// counts are immediates, multiples of 8 in [24, 256], and the CTA's total must stay within the
+// registers it was launched with.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // Named barrier over `count` threads (a multiple of 32).
