@@ -11,14 +11,11 @@
 // FlashAttention post, "Block-Sparse FlashAttention").
 //
 // GB300 mapping (prior art on the pages is A100 mma.sync with warp split-Q; not used here):
-//   CTA = two query tiles of one head (256 rows), 384 threads, one CTA per SM:
+//   CTA = two query tiles of one head (256 rows), 320 threads, one CTA per SM:
 //     warp 0       TMA producer: Q tiles once, then K_j and V_j into a ring of smem slots
 //     warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS), O_t += P_t V_j (TS, P in TMEM)
-//     warps 2, 3   idle (they complete the first warpgroup)
-//     warps 4..7   softmax for query tile 0, one TMEM lane (= query row) per thread
-//     warps 8..11  softmax for query tile 1
-//   The first warpgroup gives registers up (80 each) so the softmax warpgroups can hold 208:
-//   each softmax pass keeps 64 scores plus eight-way partial maxima / sums in registers.
+//     warps 2..5   softmax for query tile 0, one TMEM lane (= query row) per thread
+//     warps 6..9   softmax for query tile 1
 //   TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
 //   P_t is written as packed 16-bit pairs over the first 64 columns of S_t and read from
 //   there by the PV MMA, so P never touches shared memory.
@@ -49,7 +46,7 @@ struct FwdLayout {
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
-    static constexpr int kThreads = 384;
+    static constexpr int kThreads = 320;
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -75,7 +72,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
     using L = FwdLayout<D>;
@@ -133,7 +130,6 @@ __global__ void __launch_bounds__(384, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
-        regs_dec<80>();
         if (lane == 0) {
             uint8_t *sQ = smem + L::kQOff;
             mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
@@ -175,7 +171,6 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        regs_dec<80>();
         if (lane == 0) {
             const uint32_t sQ = smem_u32(smem + L::kQOff);
             const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
@@ -287,12 +282,9 @@ __global__ void __launch_bounds__(384, 1)
             drain_wait(drain, 0, p.ctl);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        regs_dec<80>();  // warps 2 and 3 only complete the first warpgroup
     } else {
         // ---------------------------------------------------------------- softmax groups
-        regs_inc<208>();
-        const int t = (warp - 4) >> 2;
+        const int t = (warp - 2) >> 2;
         const int quad = warp & 3;  // a warp may touch TMEM lanes [32*(warp%4), +32)
         const int row = quad * 32 + lane;
         const int qt = t == 0 ? qt0 : qt1;
@@ -312,38 +304,25 @@ __global__ void __launch_bounds__(384, 1)
                 break;
             }
             tc_fence_after();
-            // Two passes over 64-column halves keep the registers free for instruction-level
-            // parallelism: pass 1 takes the row max in eight independent chains, pass 2 reloads
-            // each half and turns it into P (eight partial sums for l).
+            uint32_t r[128];
+            tmem_ld32(tS + 0, r + 0);
+            tmem_ld32(tS + 32, r + 32);
+            tmem_ld32(tS + 64, r + 64);
+            tmem_ld32(tS + 96, r + 96);
+            tmem_wait_ld();
             const int kv0 = j * kTile;
             const bool need_mask = (p.causal && j == qt) || (kv0 + kTile > p.N);
-            // key kv0 + c is visible to this row iff c <= last (key < N, and key <= row if causal)
-            const int last = min(p.N - 1, p.causal ? q_row : p.N - 1) - kv0;
-            auto load_half = [&](int hh, uint32_t *r) {
-                tmem_ld32(tS + 64 * hh, r);
-                tmem_ld32(tS + 64 * hh + 32, r + 32);
-                tmem_wait_ld();
-                if (need_mask) {
-                    const int lim = last - 64 * hh;
+            float mx = -INFINITY;
+            if (need_mask) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c > lim) r[c] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 128; ++c) {
+                    const int col = kv0 + c;
+                    if (col >= p.N || (p.causal && col > q_row)) r[c] = __float_as_uint(-INFINITY);
+                    mx = fmaxf(mx, __uint_as_float(r[c]));
                 }
-            };
-            float mx;
-            {
-                float m8[8];
-                uint32_t r[64];
-                load_half(0, r);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(r[e]);
-#pragma unroll
-                for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
-                load_half(1, r);
-#pragma unroll
-                for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
-                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c]));
             }
             const float m_tile = mx * sl2;
             const float m_new = fmaxf(m, m_tile);
@@ -357,23 +336,21 @@ __global__ void __launch_bounds__(384, 1)
             }
             const bool rescale = grow && old_finite;
             const float mu = m == -INFINITY ? 0.f : m;  // a row with nothing unmasked yet
-            float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                uint32_t r[64];
-                load_half(h, r);  // P of half 0 lands over S columns [0, 32): half 1 is intact
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float a = ex2(fmaf(__uint_as_float(r[2 * c]), sl2, -mu));
-                    const float b = ex2(fmaf(__uint_as_float(r[2 * c + 1]), sl2, -mu));
-                    rs[(2 * c) & 7] += a;
-                    rs[(2 * c + 1) & 7] += b;
+                    const float a = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c]), sl2, -mu));
+                    const float b = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c + 1]), sl2, -mu));
+                    rs0 += a;
+                    rs1 += b;
                     pk[c] = pack2<BF16>(a, b);
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            l += rs0 + rs1;
             if (__any_sync(0xffffffffu, rescale)) {
                 // The previous PV into O_t has completed (its commit preceded this S_t) and the
                 // next one waits for p_full, so O_t is ours to rescale here.
