@@ -39,11 +39,15 @@ from exact_attention_staged_gb300.workloads import WORKLOADS, workload_inputs  #
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
 L2_BYTES = 129e6  # GB300 L2 (129 MB)
+_CSRC = "exact_attention_staged_gb300/csrc/"
+_SHARED = (_CSRC + "sm100.cuh", _CSRC + "fa_internal.h")
+# Files whose content decides each kernel's code: a stored ncu traffic figure is used only
+# while their combined hash still matches the one recorded with it.
 KERNEL_SOURCES = {
-    "fa_fwd_kernel": "exact_attention_staged_gb300/csrc/fa_fwd.cu",
-    "fa_bwd_dkdv_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
-    "fa_bwd_dq_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
-    "fa_bwd_preprocess_kernel": "exact_attention_staged_gb300/csrc/fa_bwd.cu",
+    "fa_fwd_kernel": (_CSRC + "fa_fwd.cu",) + _SHARED,
+    "fa_bwd_dkdv_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
+    "fa_bwd_dq_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
+    "fa_bwd_preprocess_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
 }
 
 
@@ -69,9 +73,12 @@ def measured_peaks():
                 "source": "fallback"}
 
 
-def source_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(rels):
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel, workload):
