@@ -10,6 +10,7 @@ Recipe (one per workload):
     cast of the doubled value equals the double of the cast value).
   * The block-sparse workload's 128x128 block mask: generator seeded with ``seed + 1000``;
     off-diagonal blocks kept iid with probability 0.25, every diagonal block kept.
+  * Grouped-query workloads draw K and V with H_kv heads ([B, H_kv, N, d]); Q and dO keep H.
 
 The five workloads follow the shapes of the FlashAttention-2 reading notes' kernel benchmark
 (seq 512-16k, hidden 2048, heads of 64/128) and the GPT-style 8k training shape the notes quote.
@@ -38,6 +39,11 @@ class Workload:
     qk_mult: float = 1.0  # multiplier applied to Q and K before the cast
     sparse_p: Optional[float] = None  # Bernoulli keep-probability of off-diagonal mask blocks
     backward: bool = True
+    h_kv: Optional[int] = None  # K/V heads (grouped-query attention); None means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.h_kv is None else self.h_kv
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -54,7 +60,8 @@ class Workload:
     def describe(self) -> str:
         kind = "block-sparse" if self.sparse_p is not None else ("causal" if self.causal else "dense")
         passes = "fwd+bwd" if self.backward else "fwd"
-        return (f"{self.name}: {passes} {kind} B={self.B} H={self.H} N={self.N} d={self.d} "
+        heads = f"H={self.H}" if self.h_kv is None else f"H={self.H} H_kv={self.h_kv}"
+        return (f"{self.name}: {passes} {kind} B={self.B} {heads} N={self.N} d={self.d} "
                 f"{self.dtype}")
 
 
@@ -71,21 +78,28 @@ WORKLOADS: Dict[str, Workload] = {
     # block-sparse head-64 forward+backward at 16k tokens, density about 0.256
     "blocksparse_d64_n16k": Workload("blocksparse_d64_n16k", 1, 8, 16384, 64, "bf16", False, 5,
                                      sparse_p=0.25),
+    # the GPT-style 8k shape with grouped K/V heads: 32 query heads over 8 K/V heads
+    "gqa_causal_d128_n8k": Workload("gqa_causal_d128_n8k", 1, 32, 8192, 128, "bf16", True, 6,
+                                    qk_mult=2.0, h_kv=8),
 }
 
+# the five workloads of the method's scope, in order; the rest extend it (grouped K/V heads)
 ORDER = ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k", "gpt_causal_d128_n8k",
          "blocksparse_d64_n16k"]
+EXTENSIONS = ["gqa_causal_d128_n8k"]
 
 
 def make_inputs(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
-                qk_mult: float = 1.0, with_dout: bool = True) -> Dict[str, torch.Tensor]:
+                qk_mult: float = 1.0, with_dout: bool = True,
+                h_kv: Optional[int] = None) -> Dict[str, torch.Tensor]:
     """Draw Q, K, V (and dO) on the CPU from one seeded generator, in that order."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     shape = (B, H, N, d)
+    kv_shape = (B, H if h_kv is None else h_kv, N, d)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
     out = {}
     if qk_mult != 1.0:
         q = q * qk_mult
@@ -110,7 +124,8 @@ def make_block_mask(tiles: int, seed: int, p: float, keep_diagonal: bool = True)
 
 
 def workload_inputs(w: Workload) -> Dict[str, torch.Tensor]:
-    out = make_inputs(w.B, w.H, w.N, w.d, w.torch_dtype, w.seed, w.qk_mult, with_dout=True)
+    out = make_inputs(w.B, w.H, w.N, w.d, w.torch_dtype, w.seed, w.qk_mult, with_dout=True,
+                      h_kv=w.h_kv)
     if w.sparse_p is not None:
         out["block_mask"] = make_block_mask(w.tiles, w.seed + 1000, w.sparse_p)
     return out

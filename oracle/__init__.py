@@ -176,3 +176,32 @@ def scores(q, k, scale: float, causal: bool = False, block_mask=None, block: int
 def probabilities(q, k, scale: float, causal: bool = False, block_mask=None, block: int = 128):
     """P = softmax(S) of ONE head (three-pass safe softmax)."""
     return _square("oracle_probabilities", q, k, scale, causal, block_mask, block)
+
+
+def attention_gqa(q, k, v, scale: float, causal: bool = False, block_mask=None, block: int = 128,
+                  dout=None) -> dict:
+    """Grouped-query attention: q [B, H, N, d]; k, v [B, H_kv, N, d] with H_kv dividing H.
+
+    FlashAttention-2 reading notes, section on MQA/GQA support: query head h reads the K/V head
+    of its group, and because a K/V head is shared by the query heads of its group, its
+    gradients dK, dV are the sums of theirs.  Group g holds the H / H_kv consecutive query heads
+    h with h // (H / H_kv) == g (H_kv = 1 is MQA, H_kv = H is MHA).  Written as the plain
+    definition: K and V are indexed per query head and the MHA oracle runs on that, then the
+    per-query-head dK and dV are summed over each group.
+    """
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    if qa.ndim != 4 or ka.ndim != 4 or ka.shape != va.shape or qa.shape[0] != ka.shape[0] \
+            or qa.shape[3] != ka.shape[3]:
+        raise ValueError("q must be [B, H, N, d] and k, v [B, H_kv, N, d]")
+    B, H, Nq, d = qa.shape
+    Hkv, Nk = ka.shape[1], ka.shape[2]
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError("H_kv must divide H")
+    rep = H // Hkv
+    kv_head = np.arange(H) // rep
+    res = attention(qa, np.ascontiguousarray(ka[:, kv_head]), np.ascontiguousarray(va[:, kv_head]),
+                    scale, causal, block_mask, block, dout)
+    if dout is not None:
+        res["dk"] = res["dk"].reshape(B, Hkv, rep, Nk, d).sum(axis=2)
+        res["dv"] = res["dv"].reshape(B, Hkv, rep, Nk, d).sum(axis=2)
+    return res

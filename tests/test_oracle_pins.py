@@ -311,3 +311,95 @@ def test_accepts_seeded_low_precision_inputs_exactly():
     # the bf16 values are carried into fp64 without change
     S = 0.35 * q[0, 1] @ t["k"].double().numpy()[0, 1].T
     np.testing.assert_allclose(res["lse"][0, 1], scipy.special.logsumexp(S, axis=1), atol=1e-12)
+
+
+# ---------------------------------------------------------------- grouped-query attention
+# FlashAttention-2 reading notes, MQA/GQA section: query head h uses K/V head h // (H / H_kv),
+# and the gradient of a shared K/V head is the sum over its query heads.
+
+def _gqa_torch(q, k, v, do, scale, causal):
+    """Independent fp64 autograd: every query head indexes its K/V head directly (no expansion,
+    no explicit group sum: autograd accumulates the shared leaves' gradients itself)."""
+    B, H, N, d = q.shape
+    rep = H // k.shape[1]
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    outs, lses = [], []
+    i = torch.arange(N)
+    for h in range(H):
+        S = scale * tq[:, h] @ tk[:, h // rep].transpose(-1, -2)
+        if causal:
+            S = S.masked_fill(i[None, :] > i[:, None], float("-inf"))
+        outs.append(torch.softmax(S, dim=-1) @ tv[:, h // rep])
+        lses.append(torch.logsumexp(S, dim=-1))
+    O = torch.stack(outs, dim=1)
+    O.backward(torch.tensor(do))
+    return (O.detach().numpy(), torch.stack(lses, 1).detach().numpy(), tq.grad.numpy(),
+            tk.grad.numpy(), tv.grad.numpy())
+
+
+@pytest.mark.parametrize("H,Hkv,causal", [(4, 2, False), (6, 3, True), (4, 1, True),
+                                           (3, 3, False)])
+def test_gqa_matches_per_head_torch_autograd(H, Hkv, causal):
+    B, N, d = 2, 20, 8
+    q, do = rand((B, H, N, d), 80), rand((B, H, N, d), 81)
+    k, v = rand((B, Hkv, N, d), 82), rand((B, Hkv, N, d), 83)
+    res = oracle.attention_gqa(q, k, v, 0.45, causal, dout=do)
+    o, lse, dq, dk, dv = _gqa_torch(q, k, v, do, 0.45, causal)
+    np.testing.assert_allclose(res["o"], o, atol=1e-12)
+    np.testing.assert_allclose(res["lse"], lse, atol=1e-12)
+    for name, ref in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(res[name], ref, atol=1e-11)
+
+
+def test_gqa_with_one_head_per_group_is_mha():
+    q, k, v, do = (rand((2, 3, 17, 4), s) for s in (84, 85, 86, 87))
+    a = oracle.attention_gqa(q, k, v, 0.6, True, dout=do)
+    b = oracle.attention(q, k, v, 0.6, True, dout=do)
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[name], b[name])
+
+
+def test_mqa_with_identical_query_heads_scales_kv_gradients():
+    # all H query heads equal (and their dO equal): every head produces the same dK, dV, so the
+    # shared head's gradients are exactly H times one head's, while O and dQ repeat per head
+    H, N, d = 5, 12, 4
+    q1, do1 = rand((1, 1, N, d), 88), rand((1, 1, N, d), 89)
+    k, v = rand((1, 1, N, d), 90), rand((1, 1, N, d), 91)
+    q, do = np.repeat(q1, H, axis=1), np.repeat(do1, H, axis=1)
+    many = oracle.attention_gqa(q, k, v, 0.8, False, dout=do)
+    one = oracle.attention(q1, k, v, 0.8, False, dout=do1)
+    np.testing.assert_allclose(many["dk"], H * one["dk"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(many["dv"], H * one["dv"], rtol=1e-13, atol=1e-14)
+    for h in range(H):
+        np.testing.assert_array_equal(many["o"][:, h], one["o"][:, 0])
+        np.testing.assert_array_equal(many["dq"][:, h], one["dq"][:, 0])
+
+
+def test_gqa_gradients_match_central_differences():
+    B, H, Hkv, N, d = 1, 4, 2, 6, 3
+    q, do = rand((B, H, N, d), 92), rand((B, H, N, d), 93)
+    k, v = rand((B, Hkv, N, d), 94), rand((B, Hkv, N, d), 95)
+    res = oracle.attention_gqa(q, k, v, 0.9, True, dout=do)
+
+    def loss(kk, vv):
+        return float(np.sum(oracle.attention_gqa(q, kk, vv, 0.9, True)["o"] * do))
+
+    h = 1e-6
+    for name, x, g in (("k", k, res["dk"]), ("v", v, res["dv"])):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            if name == "k":
+                fd[idx] = (loss(xp, v) - loss(xm, v)) / (2 * h)
+            else:
+                fd[idx] = (loss(k, xp) - loss(k, xm)) / (2 * h)
+        err = np.linalg.norm(fd - g) / np.linalg.norm(g)
+        assert err <= 1e-6, (name, err)
+
+
+def test_gqa_rejects_heads_that_do_not_divide():
+    with pytest.raises(ValueError):
+        oracle.attention_gqa(rand((1, 4, 8, 4), 1), rand((1, 3, 8, 4), 2), rand((1, 3, 8, 4), 3),
+                             0.5)

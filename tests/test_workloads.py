@@ -1,12 +1,12 @@
 """Seeded workload generator: shapes, determinism and the block-mask recipe (CPU only)."""
 import torch
 
-from exact_attention_staged_gb300.workloads import (ORDER, WORKLOADS, make_block_mask,
-                                                    make_inputs, workload_inputs)
+from exact_attention_staged_gb300.workloads import (EXTENSIONS, ORDER, WORKLOADS,
+                                                    make_block_mask, make_inputs, workload_inputs)
 
 
 def test_five_workloads_in_order():
-    assert ORDER == list(WORKLOADS)
+    assert ORDER + EXTENSIONS == list(WORKLOADS)
     shapes = [(WORKLOADS[n].B, WORKLOADS[n].H, WORKLOADS[n].N, WORKLOADS[n].d) for n in ORDER]
     assert shapes == [(1, 1, 128, 64), (4, 16, 1024, 64), (2, 16, 4096, 128),
                       (1, 32, 8192, 128), (1, 8, 16384, 64)]
@@ -49,3 +49,11 @@ def test_block_mask_recipe():
 def test_small_workload_inputs():
     t = workload_inputs(WORKLOADS["tiny_fwd_fp16"])
     assert t["q"].dtype == torch.float16 and t["q"].shape == (1, 1, 128, 64)
+
+
+def test_grouped_kv_heads_shapes():
+    w = WORKLOADS["gqa_causal_d128_n8k"]
+    assert (w.H, w.kv_heads, w.N, w.d) == (32, 8, 8192, 128) and w.causal
+    a = make_inputs(2, 6, 40, 8, torch.bfloat16, seed=9, h_kv=2)
+    assert a["q"].shape == (2, 6, 40, 8) and a["do"].shape == (2, 6, 40, 8)
+    assert a["k"].shape == (2, 2, 40, 8) and a["v"].shape == (2, 2, 40, 8)
