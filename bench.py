@@ -180,7 +180,9 @@ def oracle_sample(w, inputs, head=0):
     """Time the fp64 oracle (forward + backward) on one whole head of the workload."""
     import oracle
     b, h = divmod(head, w.H)
-    sl = {x: inputs[x][b, h].clone() for x in ("q", "k", "v", "do")}
+    hk = h // (w.H // w.kv_heads)  # the K/V head this query head reads
+    sl = {x: inputs[x][b, h].clone() for x in ("q", "do")}
+    sl.update({x: inputs[x][b, hk].clone() for x in ("k", "v")})
     mask = inputs.get("block_mask")
     t0 = time.perf_counter()
     oracle.attention(sl["q"], sl["k"], sl["v"], w.scale, w.causal, mask, dout=sl["do"])
@@ -249,19 +251,46 @@ def run_gpu(args, w):
     density = 1.0 if mask_cpu is None else float(mask_cpu.float().mean())
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream()
-    names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel",
-             "fa_bwd_dq_kernel"]
+    gqa = w.h_kv is not None
+    if gqa:
+        # grouped K/V heads: the forward kernel, then the whole grouped backward call (D, dK/dV
+        # summed over each group, dQ), timed as one unit
+        names = ["fa_fwd_kernel", "fa_bwd_gqa"]
+        workspace = torch.empty(api.gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d),
+                                dtype=torch.uint8, device=dev)
+        delta = workspace
+    else:
+        names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel",
+                 "fa_bwd_dq_kernel"]
+        delta = torch.empty_like(lse)
+
+    def fwd_call():
+        if gqa:
+            api.fwd_gqa(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
+        else:
+            api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
+
+    def bwd_call():
+        if gqa:
+            api.bwd_gqa(q, k, v, o, lse, do, w.scale, w.causal, mask, dq=dq, dk=dk, dv=dv,
+                        workspace=workspace)
+        else:
+            api.bwd(q, k, v, o, lse, do, w.scale, w.causal, mask, dq=dq, dk=dk, dv=dv,
+                    workspace=delta)
 
     def step(events=None):
         def mark(i):
             if events is not None:
                 events[i].record(stream)
         mark(0)
-        api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
+        fwd_call()
         mark(1)
+        if gqa:
+            bwd_call()
+            mark(2)
+            return
         api.bwd_preprocess(o, do, delta)
         mark(2)
         api.bwd_dkdv(q, k, v, do, lse, delta, dk, dv, w.scale, w.causal, mask)
@@ -275,7 +304,8 @@ def run_gpu(args, w):
     if api.sync_status() != 0:
         raise RuntimeError("device status reported an error during warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+          for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist_barrier(world)
     torch.cuda.synchronize()
@@ -291,6 +321,9 @@ def run_gpu(args, w):
         raise RuntimeError("device status reported an error in the timed region")
     max_ms = dist_max(elapsed_ms, world, dev)
     f = flops(w.B, w.H, w.N, w.d, w.causal, density)
+    if gqa:
+        f = {"fa_fwd_kernel": f["fa_fwd_kernel"],
+             "fa_bwd_gqa": sum(f.values()) - f["fa_fwd_kernel"]}
     step_flops = sum(f.values())
     value = world * step_flops * args.steps / (max_ms / 1e3) / 1e12
     per_kernel = {}
@@ -312,7 +345,8 @@ def run_gpu(args, w):
     # ---- end to end through the C ABI from pinned host buffers
     e2e_steps = max(1, min(args.steps, 5))
     hq, hk, hv, hdo = (t[x].pin_memory() for x in ("q", "k", "v", "do"))
-    ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+    ho, hdq = (torch.empty_like(hq).pin_memory() for _ in range(2))
+    hdk, hdv = (torch.empty_like(hk).pin_memory() for _ in range(2))
     hlse = torch.empty(w.B, w.H, w.N, dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
     d2h = sum(x.numel() * x.element_size() for x in (ho, hdq, hdk, hdv, hlse))
@@ -322,9 +356,8 @@ def run_gpu(args, w):
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         do.copy_(hdo, non_blocking=True)
-        api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
-        api.bwd(q, k, v, o, lse, do, w.scale, w.causal, mask, dq=dq, dk=dk, dv=dv,
-                workspace=delta)
+        fwd_call()
+        bwd_call()
         ho.copy_(o, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
         hdq.copy_(dq, non_blocking=True)
@@ -345,6 +378,10 @@ def run_gpu(args, w):
         raise RuntimeError("device status reported an error in the end-to-end loop")
     e2e_value = world * step_flops * e2e_steps / (e2e_ms / 1e3) / 1e12
 
+    launches_per_step = 4  # fwd, D, dK/dV, dQ (+ the group reduce when dK/dV is split)
+    if gqa and api.gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d) > \
+            api.workspace_bytes(w.B, w.H, w.N, w.d):
+        launches_per_step = 5
     if rank != 0:
         return 0
     cpu = None
@@ -356,7 +393,8 @@ def run_gpu(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "H_kv": w.kv_heads, "N": w.N,
+                   "d": w.d,
                    "causal": w.causal, "block_density": density,
                    "l2": f"inputs larger than L2 (step working set {ws / 1e6:.0f} MB vs "
                          f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
@@ -372,7 +410,7 @@ def run_gpu(args, w):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

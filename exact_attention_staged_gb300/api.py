@@ -25,9 +25,13 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i,
                     _f, _i, _vp, _vp]),
+    "fa_bwd_gqa_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i,
+                        _i, _i, _f, _i, _vp, _vp]),
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fa_bwd_dkdv": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
                          _vp, _vp]),
@@ -39,6 +43,7 @@ SIGNATURES = {
     "fa_debug_set_visit_log": (_i, [_vp, _sz]),
     "fa_debug_set_wait_limit_ns": (_i, [ctypes.c_ulonglong]),
     "fa_debug_set_fault": (_i, [_i]),
+    "fa_debug_set_dkdv_splits": (_i, [_i]),
 }
 
 _lib = None
@@ -193,6 +198,66 @@ def bwd_dq(q, k, v, dout, lse, delta, dq, scale=None, causal=False, block_mask=N
     return dq
 
 
+def _kv_check(q, k, v):
+    """K, V of grouped-query attention: [B, H_kv, N, d] with H_kv dividing H; returns H_kv."""
+    B, H, N, d = _shape(q)
+    for name, t in (("k", k), ("v", v)):
+        if t.dim() != 4 or t.dtype != q.dtype or t.shape[0] != B or t.shape[2:] != q.shape[2:]:
+            raise ValueError(f"{name} must be [B, H_kv, N, d] with the dtype of q")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    return int(k.shape[1])
+
+
+def fwd_gqa(q, k, v, scale: Optional[float] = None, causal: bool = False, block_mask=None,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O, LSE = grouped-query attention forward (fa_fwd_gqa): k, v are [B, H_kv, N, d]."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    Hkv = _kv_check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be fp32 [B, H, N]")
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_fwd_gqa(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
+                          _dev(lse, "lse"), B, H, Hkv, N, d, _dtype_code(q), float(scale),
+                          int(bool(causal)), mask_ptr, _stream(stream)), "fa_fwd_gqa")
+    return out, lse
+
+
+def gqa_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_gqa_workspace_bytes(B, H, H_kv, N, d))
+
+
+def bwd_gqa(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool = False,
+            block_mask=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV = grouped-query attention backward (fa_bwd_gqa); dk, dv are [B, H_kv, N, d]."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    Hkv = _kv_check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = gqa_workspace_bytes(B, H, Hkv, N, d)
+    if nbytes == 0:
+        raise ValueError("invalid grouped-query sizes")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_bwd_gqa(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o", q),
+                          _dev(dout, "dout", q), _dev(lse, "lse"), _dev(dq, "dq", q),
+                          _dev(dk, "dk", k), _dev(dv, "dv", k), _dev(workspace, "workspace"),
+                          nbytes, B, H, Hkv, N, d, _dtype_code(q), float(scale),
+                          int(bool(causal)), mask_ptr, _stream(stream)), "fa_bwd_gqa")
+    return dq, dk, dv
+
+
 def sync_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(load().fa_sync_status(_stream(stream)))
@@ -214,3 +279,7 @@ def debug_set_wait_limit_ns(ns: int):
 
 def debug_set_fault(mode: int):
     _check(load().fa_debug_set_fault(int(mode)), "fa_debug_set_fault")
+
+
+def debug_set_dkdv_splits(splits: int):
+    _check(load().fa_debug_set_dkdv_splits(int(splits)), "fa_debug_set_dkdv_splits")

@@ -22,6 +22,7 @@ uint8_t *g_visit_log = nullptr;
 size_t g_visit_bytes = 0;
 unsigned long long g_wait_ns = kDefaultWaitNs;
 int g_fault_mode = 0;
+int g_dkdv_splits = 0;  // 0: automatic
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // Device status word address and architecture check, once per device.
@@ -107,20 +108,66 @@ int make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int dtype) 
 
 int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 
-// Heads per CTA-order group: the streamed tiles of one head (two [N, d] 16-bit tensors) times
-// the group stay near 32 MiB, a quarter of the L2.
-int head_group(int BH, int N, int d) {
-    const double per_head = 4.0 * N * d;
-    int g = static_cast<int>((32.0 * 1024 * 1024) / per_head);
+int check_heads(int H, int Hkv) {
+    return (Hkv >= 1 && Hkv <= H && H % Hkv == 0) ? FA_OK : FA_ERR_INVALID;
+}
+
+// CTA-order group size: `units` work-unit heads, each streaming `tensors_per_unit` [N, d]
+// 16-bit tensors; the group's streamed tiles stay near 32 MiB, a quarter of the L2.
+int head_group(int units, int N, int d, double tensors_per_unit) {
+    const double per_unit = 2.0 * N * d * tensors_per_unit;
+    int g = static_cast<int>((32.0 * 1024 * 1024) / per_unit);
     if (g < 1) g = 1;
-    if (g > BH) g = BH;
+    if (g > units) g = units;
     return g;
 }
 
+// How the dK/dV kernel spreads the H / H_kv query heads of one K/V head: over `splits` CTAs
+// per key tile, `chunk` heads each, aiming at no fewer than kDkvTargetCtas CTAs (a few per SM)
+// so that few K/V heads (MQA) still fill the GPU.  One split needs no partial sums.
+constexpr long kDkvTargetCtas = 512;
+struct DkvSplit {
+    int splits, chunk;
+};
+DkvSplit dkdv_split(int B, int H, int Hkv, int N) {
+    const int rep = H / Hkv;
+    int s = 1;
+    if (rep > 1) {
+        int forced;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            forced = g_dkdv_splits;
+        }
+        if (forced > 0) {
+            s = forced;
+        } else {
+            const long units = static_cast<long>(B) * Hkv * tiles_of(N);
+            s = static_cast<int>((kDkvTargetCtas + units - 1) / units);
+        }
+        if (s > rep) s = rep;
+        if (s < 1) s = 1;
+    }
+    const int chunk = (rep + s - 1) / s;
+    return {(rep + chunk - 1) / chunk, chunk};
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+size_t delta_bytes(int B, int H, int N) {
+    return round256(static_cast<size_t>(B) * H * N * sizeof(float));
+}
+
+size_t part_bytes(const DkvSplit &sp, int B, int Hkv, int N, int d) {
+    if (sp.splits == 1) return 0;
+    return 2ull * sp.splits * static_cast<size_t>(B) * Hkv * N * d * sizeof(float);
+}
+
 int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-               int N, int d, int dtype, float scale, int causal, const uint8_t *mask,
+               int Hkv, int N, int d, int dtype, float scale, int causal, const uint8_t *mask,
                void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_heads(H, Hkv);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, o, lse});
     if (rc != FA_OK) return rc;
@@ -129,8 +176,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     if (rc != FA_OK) return rc;
     fa::Maps maps;
     const int BH = B * H;
-    if (make_map(&maps.q, q, BH, N, d, dtype) || make_map(&maps.k, k, BH, N, d, dtype) ||
-        make_map(&maps.v, v, BH, N, d, dtype))
+    if (make_map(&maps.q, q, BH, N, d, dtype) || make_map(&maps.k, k, B * Hkv, N, d, dtype) ||
+        make_map(&maps.v, v, B * Hkv, N, d, dtype))
         return FA_ERR_CUDA;
     fa::FwdParams p;
     p.o = o;
@@ -140,7 +187,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     p.N = N;
     p.T = tiles_of(N);
     p.num_pairs = (p.T + 1) / 2;
-    p.head_group = head_group(BH, N, d);
+    p.rep = H / Hkv;
+    p.head_group = head_group(BH, N, d, 2.0 / p.rep);  // K and V, shared by rep query heads
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
     if (make_ctl(status, BH, p.T, &p.ctl) != FA_OK) return FA_ERR_INVALID;
@@ -149,9 +197,11 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
 }
 
 int bwd_params(const void *q, const void *k, const void *v, const void *dout, const float *lse,
-               const float *delta, int B, int H, int N, int d, int dtype, float scale,
+               const float *delta, int B, int H, int Hkv, int N, int d, int dtype, float scale,
                int causal, const uint8_t *mask, fa::Maps *maps, fa::BwdParams *p) {
     int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_heads(H, Hkv);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, dout, lse, delta});
     if (rc != FA_OK) return rc;
@@ -159,8 +209,9 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
     rc = device_setup(&dev, &status);
     if (rc != FA_OK) return rc;
     const int BH = B * H;
-    if (make_map(&maps->q, q, BH, N, d, dtype) || make_map(&maps->k, k, BH, N, d, dtype) ||
-        make_map(&maps->v, v, BH, N, d, dtype) || make_map(&maps->dout, dout, BH, N, d, dtype))
+    if (make_map(&maps->q, q, BH, N, d, dtype) || make_map(&maps->k, k, B * Hkv, N, d, dtype) ||
+        make_map(&maps->v, v, B * Hkv, N, d, dtype) ||
+        make_map(&maps->dout, dout, BH, N, d, dtype))
         return FA_ERR_CUDA;
     p->out0 = nullptr;
     p->out1 = nullptr;
@@ -170,11 +221,90 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
     p->BH = BH;
     p->N = N;
     p->T = tiles_of(N);
-    p->head_group = head_group(BH, N, d);
+    p->rep = H / Hkv;
+    p->head_group = head_group(BH, N, d, 2.0 / p->rep);  // dQ: K and V per query head
+    p->units = BH;
+    p->splits = 1;
+    p->chunk = p->rep;
+    p->part = nullptr;
+    p->kv_elems = static_cast<long>(B) * Hkv * N * d;
     p->scale = scale;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->causal = causal ? 1 : 0;
     return make_ctl(status, BH, p->T, &p->ctl);
+}
+
+// dK/dV (+ the group reduce when the K/V groups are split, sp.splits > 1); part: room for
+// part_bytes(sp, ...) of fp32 partial sums, or nullptr with one split.
+int run_dkdv(const void *q, const void *k, const void *v, const void *dout, const float *lse,
+             const float *delta, void *dk, void *dv, const DkvSplit &sp, float *part, int B,
+             int H, int Hkv, int N, int d, int dtype, float scale, int causal,
+             const uint8_t *mask, void *stream) {
+    fa::Maps maps;
+    fa::BwdParams p;
+    int rc = bwd_params(q, k, v, dout, lse, delta, B, H, Hkv, N, d, dtype, scale, causal, mask,
+                        &maps, &p);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({dk, dv});
+    if (rc != FA_OK) return rc;
+    if (sp.splits < 1 || sp.chunk < 1 || sp.splits * sp.chunk < H / Hkv) return FA_ERR_INVALID;
+    if (sp.splits > 1 && (part == nullptr || !aligned16(part))) return FA_ERR_INVALID;
+    p.out0 = dk;
+    p.out1 = dv;
+    p.splits = sp.splits;
+    p.chunk = sp.chunk;
+    p.units = B * Hkv * sp.splits;
+    p.part = sp.splits > 1 ? part : nullptr;
+    p.head_group = head_group(p.units, N, d, 2.0 * sp.chunk);  // Q and dO of chunk heads
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fa::launch_bwd_dkdv(maps, p, d, dtype == FA_BF16, st);
+    if (e == cudaSuccess && sp.splits > 1)
+        e = fa::launch_bwd_group_reduce(part, dk, dv, sp.splits, p.kv_elems, dtype == FA_BF16, st);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int run_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
+           const float *delta, void *dq, int B, int H, int Hkv, int N, int d, int dtype,
+           float scale, int causal, const uint8_t *mask, void *stream) {
+    fa::Maps maps;
+    fa::BwdParams p;
+    int rc = bwd_params(q, k, v, dout, lse, delta, B, H, Hkv, N, d, dtype, scale, causal, mask,
+                        &maps, &p);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({dq});
+    if (rc != FA_OK) return rc;
+    p.out0 = dq;
+    cudaError_t e =
+        fa::launch_bwd_dq(maps, p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int run_preprocess(const void *o, const void *dout, float *delta, int B, int H, int N, int d,
+                   int dtype, void *stream) {
+    int rc = check_shape(B, H, N, d, dtype, 1.f);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({o, dout, delta});
+    if (rc != FA_OK) return rc;
+    int dev = 0, *status = nullptr;
+    rc = device_setup(&dev, &status);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = fa::launch_bwd_preprocess(o, dout, delta, static_cast<long>(B) * H * N, d,
+                                              dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The whole backward: D, dK/dV (+ reduce), dQ.  delta: B*H*N floats; sp, part: see run_dkdv.
+int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+            const float *lse, void *dq, void *dk, void *dv, float *delta, const DkvSplit &sp,
+            float *part, int B, int H, int Hkv, int N, int d, int dtype, float scale, int causal,
+            const uint8_t *mask, void *stream) {
+    int rc = run_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
+    if (rc != FA_OK) return rc;
+    rc = run_dkdv(q, k, v, dout, lse, delta, dk, dv, sp, part, B, H, Hkv, N, d, dtype, scale,
+                  causal, mask, stream);
+    if (rc != FA_OK) return rc;
+    return run_dq(q, k, v, dout, lse, delta, dq, B, H, Hkv, N, d, dtype, scale, causal, mask,
+                  stream);
 }
 
 // Scratch of fa_bwd_noalloc: the D values (one float per query row) of one backward call.
@@ -201,87 +331,81 @@ extern "C" {
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
            int d, int dtype, float scale, int causal, void *stream) {
-    return fwd_common(q, k, v, o, lse, B, H, N, d, dtype, scale, causal, nullptr, stream);
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, nullptr, stream);
 }
 
 int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                        int H, int N, int d, int dtype, float scale, int causal,
                        const uint8_t *block_mask, void *stream) {
     if (block_mask == nullptr) return FA_ERR_INVALID;
-    return fwd_common(q, k, v, o, lse, B, H, N, d, dtype, scale, causal, block_mask, stream);
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, block_mask, stream);
+}
+
+int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int H_kv, int N, int d, int dtype, float scale, int causal,
+               const uint8_t *block_mask, void *stream) {
+    return fwd_common(q, k, v, o, lse, B, H, H_kv, N, d, dtype, scale, causal, block_mask,
+                      stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     (void)d;
     if (B < 1 || H < 1 || N < 1) return 0;
-    const size_t bytes = static_cast<size_t>(B) * H * N * sizeof(float);
-    return (bytes + 255) / 256 * 256;
+    return delta_bytes(B, H, N);
+}
+
+size_t fa_bwd_gqa_workspace_bytes(int B, int H, int H_kv, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || check_heads(H, H_kv) != FA_OK) return 0;
+    return delta_bytes(B, H, N) + part_bytes(dkdv_split(B, H, H_kv, N), B, H_kv, N, d);
 }
 
 int fa_bwd_preprocess(const void *o, const void *dout, float *delta, int B, int H, int N, int d,
                       int dtype, void *stream) {
-    int rc = check_shape(B, H, N, d, dtype, 1.f);
-    if (rc != FA_OK) return rc;
-    rc = check_ptrs({o, dout, delta});
-    if (rc != FA_OK) return rc;
-    int dev = 0, *status = nullptr;
-    rc = device_setup(&dev, &status);
-    if (rc != FA_OK) return rc;
-    cudaError_t e = fa::launch_bwd_preprocess(o, dout, delta, static_cast<long>(B) * H * N, d,
-                                              dtype == FA_BF16, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return run_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
 }
 
 int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dout, const float *lse,
                 const float *delta, void *dk, void *dv, int B, int H, int N, int d, int dtype,
                 float scale, int causal, const uint8_t *block_mask, void *stream) {
-    fa::Maps maps;
-    fa::BwdParams p;
-    int rc = bwd_params(q, k, v, dout, lse, delta, B, H, N, d, dtype, scale, causal, block_mask,
-                        &maps, &p);
-    if (rc != FA_OK) return rc;
-    rc = check_ptrs({dk, dv});
-    if (rc != FA_OK) return rc;
-    p.out0 = dk;
-    p.out1 = dv;
-    cudaError_t e =
-        fa::launch_bwd_dkdv(maps, p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return run_dkdv(q, k, v, dout, lse, delta, dk, dv, DkvSplit{1, 1}, nullptr, B, H, H, N, d,
+                    dtype, scale, causal, block_mask, stream);
 }
 
 int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
               const float *delta, void *dq, int B, int H, int N, int d, int dtype, float scale,
               int causal, const uint8_t *block_mask, void *stream) {
-    fa::Maps maps;
-    fa::BwdParams p;
-    int rc = bwd_params(q, k, v, dout, lse, delta, B, H, N, d, dtype, scale, causal, block_mask,
-                        &maps, &p);
-    if (rc != FA_OK) return rc;
-    rc = check_ptrs({dq});
-    if (rc != FA_OK) return rc;
-    p.out0 = dq;
-    cudaError_t e =
-        fa::launch_bwd_dq(maps, p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return run_dq(q, k, v, dout, lse, delta, dq, B, H, H, N, d, dtype, scale, causal, block_mask,
+                  stream);
 }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
            const float *lse, void *dq, void *dk, void *dv, void *workspace,
            size_t workspace_bytes, int B, int H, int N, int d, int dtype, float scale,
            int causal, const uint8_t *block_mask, void *stream) {
+    return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H, N,
+                      d, dtype, scale, causal, block_mask, stream);
+}
+
+int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const void *dout,
+               const float *lse, void *dq, void *dk, void *dv, void *workspace,
+               size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
+               float scale, int causal, const uint8_t *block_mask, void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_heads(H, H_kv);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace});
     if (rc != FA_OK) return rc;
-    if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID;
+    const size_t need_delta = delta_bytes(B, H, N);
+    const DkvSplit sp = dkdv_split(B, H, H_kv, N);  // once: the size check and the launch agree
+    const size_t need_part = part_bytes(sp, B, H_kv, N, d);
+    if (workspace_bytes < need_delta + need_part) return FA_ERR_INVALID;
     float *delta = static_cast<float *>(workspace);
-    rc = fa_bwd_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
-    if (rc != FA_OK) return rc;
-    rc = fa_bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, B, H, N, d, dtype, scale, causal,
-                     block_mask, stream);
-    if (rc != FA_OK) return rc;
-    return fa_bwd_dq(q, k, v, dout, lse, delta, dq, B, H, N, d, dtype, scale, causal, block_mask,
-                     stream);
+    float *part = need_part ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                        need_delta)
+                            : nullptr;
+    return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, sp, part, B, H, H_kv, N, d, dtype,
+                   scale, causal, block_mask, stream);
 }
 
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -298,13 +422,8 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
     float *delta = nullptr;
     rc = noalloc_scratch(dev, &delta);
     if (rc != FA_OK) return rc;
-    rc = fa_bwd_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
-    if (rc != FA_OK) return rc;
-    rc = fa_bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, B, H, N, d, dtype, scale, causal,
-                     block_mask, stream);
-    if (rc != FA_OK) return rc;
-    return fa_bwd_dq(q, k, v, dout, lse, delta, dq, B, H, N, d, dtype, scale, causal, block_mask,
-                     stream);
+    return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, DkvSplit{1, 1}, nullptr, B, H, H, N,
+                   d, dtype, scale, causal, block_mask, stream);
 }
 
 int fa_sync_status(void *stream) {
@@ -341,6 +460,13 @@ int fa_debug_set_visit_log(uint8_t *buf, size_t bytes) {
 int fa_debug_set_wait_limit_ns(unsigned long long ns) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_wait_ns = ns ? ns : kDefaultWaitNs;
+    return FA_OK;
+}
+
+int fa_debug_set_dkdv_splits(int splits) {
+    if (splits < 0) return FA_ERR_INVALID;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_dkdv_splits = splits;
     return FA_OK;
 }
 

@@ -43,6 +43,19 @@ __device__ __forceinline__ bool tile_live(const BwdParams &p, int qt, int kt) {
     return true;
 }
 
+// The dK/dV kernel walks the (query head, query tile) pairs of its key tile kt in order, query
+// tiles fastest: advance (hq, i) to the next live pair; hq reaches hq_end when none is left.
+__device__ __forceinline__ void next_unit(const BwdParams &p, int kt, int i0, int hq_end, int &hq,
+                                          int &i) {
+    for (;;) {
+        if (++i >= p.T) {
+            if (++hq >= hq_end) return;
+            i = i0;
+        }
+        if (tile_live(p, i, kt)) return;
+    }
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = global_timer_ns();
@@ -74,6 +87,15 @@ __device__ __forceinline__ void store_row32(void *dst, const uint32_t *v, float 
     d[1] = make_uint4(w[4], w[5], w[6], w[7]);
     d[2] = make_uint4(w[8], w[9], w[10], w[11]);
     d[3] = make_uint4(w[12], w[13], w[14], w[15]);
+}
+
+// Store 32 fp32 values (times `mul`) of one row as fp32, 128 bytes.
+__device__ __forceinline__ void store_row32_f32(float *dst, const uint32_t *v, float mul) {
+    float4 *d = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        d[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                           __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
 }
 
 // Store 16 fp32 values (times `mul`) of one row as 16-bit values, 32 bytes.
@@ -123,7 +145,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
 }
 
 // ================================================================================ dK / dV
-// CTA = one 128-row key tile, 576 threads: warp 0 loads, warp 1 issues the MMAs, warps 2..17
+// CTA = one 128-row key tile of one K/V head, 576 threads: warp 0 loads, warp 1 issues the MMAs, warps 2..17
 // are four compute groups, group g owning query columns [32g, 32g+32) of every score tile.
 // Shared memory: K_j and V_j (stationary), a ring of slots that receives Q_0, dO_0, Q_1, dO_1,
 // ... in that order (each released as soon as its last MMA is done), and a two-entry ring of
@@ -133,6 +155,11 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
 // MMA order, one query tile of lookahead: dV(n), S^T(n+1), dK(n), dP^T(n+1), dV(n+1), ...
 // So the exponentials of tile n+1 overlap dK(n) and dP^T(n+1), and dS(n+1) overlaps dV(n+1)
 // and S^T(n+2).  One issuing thread keeps this order exact on the tensor pipe.
+// Grouped-query attention (FlashAttention-2 reading notes, MQA/GQA section): the query tiles
+// of every query head that shares this K/V head stream through the same pipeline, one head
+// after the other, so dK and dV are summed over the group in TMEM.  When there are too few K/V
+// heads to fill the GPU, the group is split over several CTAs whose fp32 partial sums a second
+// kernel adds up (fa_bwd_group_reduce_kernel).
 template <int D>
 struct DkvLayout {
     static constexpr int kTileBytes = kTile * D * 2;
@@ -184,8 +211,11 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     float *ld_ring = reinterpret_cast<float *>(smem + L::kLdOff);
 
     const int warp = warp_id(), lane = lane_id();
-    const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.T, p.head_group);
-    const int bh = ord.head;
+    const CtaOrder ord = cta_order(blockIdx.x, p.units, p.T, p.head_group);
+    const int kvh = ord.head / p.splits;               // b * H_kv + K/V head
+    const int split = ord.head - kvh * p.splits;
+    const int hq0 = kvh * p.rep + split * p.chunk;     // first query head (b * H + h)
+    const int hq_end = min(hq0 + p.chunk, (kvh + 1) * p.rep);
     const int kt = ord.rank;           // key tile; tile 0 sees the most query tiles when causal
     const int i0 = p.causal ? kt : 0;  // first query tile that can see it
 
@@ -222,16 +252,17 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes);
             for (int b = 0; b < L::kBoxes; ++b) {
-                tma_load_3d(smem + L::kKOff + b * L::kBoxBytes, &tmk, b * 64, kt * kTile, bh,
+                tma_load_3d(smem + L::kKOff + b * L::kBoxBytes, &tmk, b * 64, kt * kTile, kvh,
                             kv_full);
-                tma_load_3d(smem + L::kVOff + b * L::kBoxBytes, &tmv, b * 64, kt * kTile, bh,
+                tma_load_3d(smem + L::kVOff + b * L::kBoxBytes, &tmv, b * 64, kt * kTile, kvh,
                             kv_full);
             }
         }
         int n = 0;  // query tiles issued
         bool ok = true;
-        for (int i = i0; i < p.T && ok; ++i) {
-            if (!tile_live(p, i, kt)) continue;
+        int hq = hq0, i = i0 - 1;
+        next_unit(p, kt, i0, hq_end, hq, i);
+        for (; hq < hq_end && ok; next_unit(p, kt, i0, hq_end, hq, i)) {
             for (int x = 0; x < 2 && ok; ++x) {  // Q_i then dO_i
                 const int l = 2 * n + x;
                 const int s = l % L::kSlots;
@@ -243,7 +274,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                         uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
                         for (int b = 0; b < L::kBoxes; ++b)
                             tma_load_3d(dst + b * L::kBoxBytes, x ? &tmdo : &tmq, b * 64,
-                                        i * kTile, bh, &full[s]);
+                                        i * kTile, hq, &full[s]);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, got, 0) != 0;
@@ -263,7 +294,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 const int c = lane + 32 * k;
                 const int row = i * kTile + c;
                 const bool in = row < p.N;
-                const size_t off = static_cast<size_t>(bh) * p.N + (in ? row : 0);
+                const size_t off = static_cast<size_t>(hq) * p.N + (in ? row : 0);
                 cp_async_4(dl + c, p.lse + off, in);
                 cp_async_4(dl + 128 + c, p.delta + off, in);
             }
@@ -307,30 +338,28 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     mma_ts(d, a_col + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(b, kk * 2048),
                            kIdescTS, (acc || kk > 0) ? 1u : 0u);
             };
-            auto next_live = [&](int i) {
-                for (++i; i < p.T; ++i)
-                    if (tile_live(p, i, kt)) return i;
-                return p.T;
-            };
-            auto log_visit = [&](int i) {
+            auto log_visit = [&](int hq, int i) {
                 if (p.ctl.visit_log != nullptr)
-                    p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + i) * p.T + kt] |= 2;
+                    p.ctl.visit_log[(static_cast<size_t>(hq) * p.T + i) * p.T + kt] |= 2;
             };
             bool ok = mbar_wait(kv_full, 0, p.ctl, abort_flag);
-            int i = next_live(i0 - 1);
+            int hq = hq0, i = i0 - 1;
+            next_unit(p, kt, i0, hq_end, hq, i);
             int n = 0;
-            if (ok && i < p.T) {
+            if (ok && hq < hq_end) {
                 ok = full_wait(0) && full_wait(1);
                 if (ok) {
                     issue_ss(tS, dK0, 0);
                     umma_commit(s_full);
                     issue_ss(tdP, dV0, 1);
                     umma_commit(dp_full);
-                    log_visit(i);
+                    log_visit(hq, i);
                 }
             }
-            while (ok && i < p.T) {
-                const int nxt = next_live(i);
+            while (ok && hq < hq_end) {
+                int nhq = hq, ni = i;
+                next_unit(p, kt, i0, hq_end, nhq, ni);
+                const bool more = nhq < hq_end;
                 const int lq = 2 * n, ldo = 2 * n + 1;  // this tile's Q and dO loads
                 if (!mbar_wait(p_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
@@ -339,14 +368,14 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 tc_fence_after();
                 issue_ts(tdV, tS, ldo, n > 0);  // dV += P^T dO
                 umma_commit(&empty[slot_of(ldo)]);
-                if (nxt < p.T) {
+                if (more) {
                     if (!full_wait(lq + 2)) {
                         ok = false;
                         break;
                     }
                     issue_ss(tS, dK0, lq + 2);  // S^T(n+1) = K Q^T
                     umma_commit(s_full);
-                    log_visit(nxt);
+                    log_visit(nhq, ni);
                 }
                 if (!mbar_wait(ds_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
@@ -355,7 +384,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 tc_fence_after();
                 issue_ts(tdK, tdP, lq, n > 0);  // dK += dS^T Q
                 umma_commit(&empty[slot_of(lq)]);
-                if (nxt < p.T) {
+                if (more) {
                     if (!full_wait(ldo + 2)) {
                         ok = false;
                         break;
@@ -363,7 +392,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     issue_ss(tdP, dV0, ldo + 2);  // dP^T(n+1) = V dO^T
                     umma_commit(dp_full);
                 }
-                i = nxt;
+                hq = nhq;
+                i = ni;
                 ++n;
             }
             if (ok && n > 0) umma_commit(fin);
@@ -382,8 +412,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         const float sl2 = p.scale_log2;
         int n = 0;
         bool ok = true;
-        for (int i = i0; i < p.T; ++i) {
-            if (!tile_live(p, i, kt)) continue;
+        int hq = hq0, i = i0 - 1;
+        next_unit(p, kt, i0, hq_end, hq, i);
+        for (; hq < hq_end; next_unit(p, kt, i0, hq_end, hq, i)) {
             const int e = n & 1;
             if (!mbar_wait_warp(&ld_full[e], (n >> 1) & 1, p.ctl, abort_flag) ||
                 !mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
@@ -456,12 +487,18 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             tc_fence_after();
         }
         if (ok) {
-            // groups 0, 1 write the two column halves of dV; groups 2, 3 those of dK (x scale)
+            // groups 0, 1 write the two column halves of dV; groups 2, 3 those of dK (x scale),
+            // as 16-bit values, or as fp32 partial sums when the K/V group is split
             const bool valid = k_row < p.N;
             using T = elem_t<BF16>;
             const int half = g & 1;
-            T *dst = reinterpret_cast<T *>(g < 2 ? p.out1 : p.out0) +
-                     (static_cast<size_t>(bh) * p.N + k_row) * D + half * (D / 2);
+            const size_t row_off =
+                (static_cast<size_t>(kvh) * p.N + k_row) * D + half * (D / 2);
+            T *dst = reinterpret_cast<T *>(g < 2 ? p.out1 : p.out0) + row_off;
+            float *dstf = p.part == nullptr ? nullptr
+                                            : p.part + (static_cast<size_t>(g < 2 ? 1 : 0) *
+                                                            p.splits + split) * p.kv_elems +
+                                                  row_off;
             const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
             const float mul = g < 2 ? 1.f : p.scale;
 #pragma unroll
@@ -474,7 +511,12 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) a[e2] = 0u;
                 }
-                if (valid) store_row32<BF16>(dst + 32 * cc, a, mul);
+                if (valid) {
+                    if (dstf != nullptr)
+                        store_row32_f32(dstf + 32 * cc, a, mul);
+                    else
+                        store_row32<BF16>(dst + 32 * cc, a, mul);
+                }
             }
         }
     }
@@ -545,6 +587,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     const int warp = warp_id(), lane = lane_id();
     const CtaOrder ord = cta_order(blockIdx.x, p.BH, p.T, p.head_group);
     const int bh = ord.head;
+    const int kvh = bh / p.rep;         // K/V head of this query head's group
     const int qt = p.T - 1 - ord.rank;  // long rows first
     const int jend = p.causal ? qt + 1 : p.T;
 
@@ -597,7 +640,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
                     for (int b = 0; b < L::kBoxes; ++b)
                         tma_load_3d(dst + b * L::kBoxBytes, x ? &tmv : &tmk, b * 64, j * kTile,
-                                    bh, &full[s]);
+                                    kvh, &full[s]);
                 }
             }
             if (!ok || *abort_flag) {
@@ -823,6 +866,41 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     }
 }
 
+// ================================================================================ group reduce
+// dK, dV of grouped-query attention whose K/V groups were split over several dK/dV CTAs:
+// the sum of the splits' fp32 partials, always added in split order (deterministic), rounded
+// once to the 16-bit output type.  8 consecutive elements per thread.
+template <bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_group_reduce_kernel(const float *part, void *dk,
+                                                                  void *dv, int splits,
+                                                                  long kv_elems) {
+    const long per = kv_elems / 8;
+    const long gid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid >= 2 * per) return;
+    const int which = gid >= per ? 1 : 0;  // 0 dK, 1 dV
+    const long e = (gid - which * per) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            part + (static_cast<long>(which) * splits + s) * kv_elems + e);
+        const float4 a = src[0], b = src[1];
+        acc[0] += a.x;
+        acc[1] += a.y;
+        acc[2] += a.z;
+        acc[3] += a.w;
+        acc[4] += b.x;
+        acc[5] += b.y;
+        acc[6] += b.z;
+        acc[7] += b.w;
+    }
+    uint4 w;
+    w.x = pack2<BF16>(acc[0], acc[1]);
+    w.y = pack2<BF16>(acc[2], acc[3]);
+    w.z = pack2<BF16>(acc[4], acc[5]);
+    w.w = pack2<BF16>(acc[6], acc[7]);
+    reinterpret_cast<uint4 *>(static_cast<elem_t<BF16> *>(which ? dv : dk) + e)[0] = w;
+}
+
 template <int D, bool BF16>
 cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long rows,
                          cudaStream_t stream) {
@@ -840,7 +918,7 @@ cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, cudaStream_t stream
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(static_cast<long>(p.BH) * p.T), L::kThreads, L::kAlloc,
+    kern<<<static_cast<unsigned>(static_cast<long>(p.units) * p.T), L::kThreads, L::kAlloc,
            stream>>>(m.q, m.k, m.v, m.dout, p);
     return cudaGetLastError();
 }
@@ -865,6 +943,18 @@ cudaError_t launch_bwd_preprocess(const void *o, const void *dout, float *delta,
                              : launch_pre_t<64, false>(o, dout, delta, rows, stream);
     return bf16 ? launch_pre_t<128, true>(o, dout, delta, rows, stream)
                 : launch_pre_t<128, false>(o, dout, delta, rows, stream);
+}
+
+cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int splits,
+                                    long kv_elems, bool bf16, cudaStream_t stream) {
+    const long threads = 2 * (kv_elems / 8);
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    if (bf16)
+        fa_bwd_group_reduce_kernel<true><<<blocks, 256, 0, stream>>>(part, dk, dv, splits, kv_elems);
+    else
+        fa_bwd_group_reduce_kernel<false><<<blocks, 256, 0, stream>>>(part, dk, dv, splits,
+                                                                      kv_elems);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf16,

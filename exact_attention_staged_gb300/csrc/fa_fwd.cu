@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
     const bool has1 = qt1 < p.T;
     const int jend = p.causal ? min(has1 ? qt1 : qt0, p.T - 1) + 1 : p.T;
+    const int kvh = bh / p.rep;  // K/V head shared by this query head's group
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(320, 1)
                         uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
                         for (int b = 0; b < L::kBoxes; ++b)
                             tma_load_3d(dst + b * L::kBoxBytes, kv ? &tmv : &tmk, b * 64,
-                                        j * kTile, bh, &full[s]);
+                                        j * kTile, kvh, &full[s]);
                     }
                     ++n;
                 }

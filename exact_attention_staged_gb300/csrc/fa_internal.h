@@ -39,19 +39,29 @@ struct FwdParams {
     int BH, N, T;             // heads (B*H), sequence length, tiles per side
     int num_pairs;            // ceil(T / 2): query-tile pairs per head
     int head_group;           // heads per CTA-order group (see cta_order)
+    int rep;                  // query heads per K/V head: K/V head of query head bh is bh / rep
     float scale_log2;         // scale * log2(e)
     int causal;
     Ctl ctl;
 };
 
 struct BwdParams {
-    void *out0;               // dK (dK/dV kernel) or dQ (dQ kernel)
+    void *out0;               // dK (dK/dV kernel, [B,H_kv,N,d]) or dQ (dQ kernel, [B,H,N,d])
     void *out1;               // dV (dK/dV kernel) or unused
     const float *lse;         // [B,H,N]
     const float *delta;       // [B,H,N]
     const uint8_t *mask;      // [T][T] or nullptr
-    int BH, N, T;
-    int head_group;           // heads per CTA-order group (see cta_order)
+    int BH, N, T;             // query heads (B*H), sequence length, tiles per side
+    int head_group;           // CTA-order group size (see cta_order)
+    int rep;                  // query heads per K/V head
+    // dK/dV only: the rep query heads of a K/V head are split over `splits` CTAs per key tile,
+    // `chunk` heads each.  With splits == 1 the kernel writes dK, dV; otherwise each split
+    // writes fp32 partial sums to part[(which * splits + split) * kv_elems + ...] (which: 0 dK,
+    // 1 dV) and fa_bwd_group_reduce_kernel adds them up.
+    int units;                // B * H_kv * splits: the "heads" of the dK/dV CTA order
+    int splits, chunk;
+    float *part;
+    long kv_elems;            // B * H_kv * N * d
     float scale;              // softmax scale (dK and dQ carry it)
     float scale_log2;         // scale * log2(e)
     int causal;
@@ -70,5 +80,7 @@ cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
                           cudaStream_t stream);
+cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int splits,
+                                    long kv_elems, bool bf16, cudaStream_t stream);
 
 }  // namespace fa

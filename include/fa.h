@@ -34,6 +34,7 @@
  *    P = exp(S - L) eq. (16) and the softmax Jacobian eq. (17); causal masking section.
  *  - FlashAttention post (bluuewhale.github.io): the 1/sqrt(d) scale ("How Attention Is
  *    Computed") and block-sparse FlashAttention ("Block-Sparse FlashAttention").
+ *  - The same reading notes, section on MQA/GQA support, for the *_gqa entry points.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -75,6 +76,19 @@ int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, flo
                        int H, int N, int d, int dtype, float scale, int causal,
                        const uint8_t *block_mask, void *stream);
 
+/*
+ * Grouped-query forward.  FlashAttention-2 reading notes, MQA/GQA section: K and V have H_kv
+ * heads, H_kv divides H, and query head h attends with K/V head h / (H / H_kv) (consecutive
+ * query heads share a K/V head; H_kv = 1 is MQA, H_kv = H is fa_fwd).  K/V are read in place,
+ * never copied per query head.
+ *   q, o       : [B,H,N,d];  k, v : [B,H_kv,N,d];  lse : [B,H,N] fp32.
+ *   block_mask : NULL for dense, otherwise as in fa_fwd_blocksparse.
+ * H_kv < 1, or H_kv not dividing H: FA_ERR_INVALID.  Other arguments as fa_fwd.
+ */
+int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int H_kv, int N, int d, int dtype, float scale, int causal,
+               const uint8_t *block_mask, void *stream);
+
 /* Bytes of device scratch fa_bwd needs: D (fp32 [B,H,N]), rounded up to 256 bytes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -93,6 +107,28 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
            const float *lse, void *dq, void *dk, void *dv, void *workspace,
            size_t workspace_bytes, int B, int H, int N, int d, int dtype, float scale,
            int causal, const uint8_t *block_mask, void *stream);
+
+/*
+ * Bytes of device scratch fa_bwd_gqa needs: D (fp32 [B,H,N], rounded up to 256 bytes) plus,
+ * when the dK/dV pass splits each K/V head's query group over several CTAs (few K/V heads, so
+ * that the GPU is still filled), fp32 partial sums of dK and dV: 2 * splits * B*H_kv*N*d floats.
+ * Returns 0 for invalid sizes.  Depends only on the arguments (and fa_debug_set_dkdv_splits).
+ */
+size_t fa_bwd_gqa_workspace_bytes(int B, int H, int H_kv, int N, int d);
+
+/*
+ * Grouped-query backward.  FlashAttention-2 reading notes, MQA/GQA section: the gradient of a
+ * shared K/V head is the sum of its query heads' gradients.  The dK/dV pass walks all query
+ * heads of a group through one accumulator in tensor memory (and, when split, adds the fp32
+ * partials in a fixed order), so the result is deterministic.
+ *   q, o, dout, dq : [B,H,N,d];  k, v, dk, dv : [B,H_kv,N,d];  lse : [B,H,N] fp32.
+ *   workspace      : at least fa_bwd_gqa_workspace_bytes() bytes, 16-byte aligned.
+ * Other arguments as fa_bwd; fa_bwd is this call with H_kv = H.
+ */
+int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const void *dout,
+               const float *lse, void *dq, void *dk, void *dv, void *workspace,
+               size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
+               float scale, int causal, const uint8_t *block_mask, void *stream);
 
 /*
  * The three stages of fa_bwd, exposed so a caller (or a profiler) can order or time them.
@@ -153,10 +189,14 @@ const char *fa_status_string(int code);
  * fa_debug_set_wait_limit_ns: bound on every device pipeline wait (default 2 s; 0 restores it).
  * fa_debug_set_fault: 0 = none; 1 = the forward's load warp skips the first key tile of each
  *   CTA, so the bounded waits run out and fa_sync_status() reports FA_ERR_TIMEOUT.
+ * fa_debug_set_dkdv_splits: 0 = automatic; s > 0 splits every K/V head's query group of
+ *   fa_bwd_gqa over min(s, H / H_kv) dK/dV CTAs per key tile (changes the workspace size).
+ *   Negative: FA_ERR_INVALID.
  */
 int fa_debug_set_visit_log(uint8_t *buf, size_t bytes);
 int fa_debug_set_wait_limit_ns(unsigned long long ns);
 int fa_debug_set_fault(int mode);
+int fa_debug_set_dkdv_splits(int splits);
 
 #ifdef __cplusplus
 }

@@ -83,3 +83,32 @@ def test_missing_library_fails_loudly(tmp_path):
             api.load(str(tmp_path / "libfa.so"))
     finally:
         api._lib = saved
+
+
+def test_gqa_workspace_and_validation(lib):
+    p = ctypes.c_void_p(16)
+    # H_kv = H needs only D; the grouped size adds the split partial sums when there are any
+    assert api.gqa_workspace_bytes(2, 16, 16, 4096, 128) == api.workspace_bytes(2, 16, 4096, 128)
+    # 32 query heads over 8 K/V heads at N = 8192: 8 * 64 key tiles fill the GPU, no split
+    assert api.gqa_workspace_bytes(1, 32, 8, 8192, 128) == 32 * 8192 * 4
+    # one K/V head over 4 query heads, 2 key tiles: every head gets its own split
+    delta = 4 * 256 * 4
+    assert api.gqa_workspace_bytes(1, 4, 1, 256, 64) == delta + 2 * 4 * 256 * 64 * 4
+    try:
+        api.debug_set_dkdv_splits(2)
+        assert api.gqa_workspace_bytes(1, 4, 1, 256, 64) == delta + 2 * 2 * 256 * 64 * 4
+        api.debug_set_dkdv_splits(1)
+        assert api.gqa_workspace_bytes(1, 4, 1, 256, 64) == delta
+        api.debug_set_dkdv_splits(99)  # capped at H / H_kv
+        assert api.gqa_workspace_bytes(1, 4, 1, 256, 64) == delta + 2 * 4 * 256 * 64 * 4
+    finally:
+        api.debug_set_dkdv_splits(0)
+    assert lib.fa_debug_set_dkdv_splits(-1) == api.FA_ERR_INVALID
+    assert lib.fa_bwd_gqa_workspace_bytes(1, 6, 4, 128, 64) == 0  # 4 does not divide 6
+    for hkv in (0, 3, 12):  # not a divisor of H = 8, or more K/V heads than query heads
+        assert lib.fa_fwd_gqa(p, p, p, p, p, 1, 8, hkv, 128, 64, 1, 0.125, 0, None,
+                              None) == api.FA_ERR_INVALID
+        assert lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, 1 << 30, 1, 8, hkv, 128, 64, 1,
+                              0.125, 0, None, None) == api.FA_ERR_INVALID
+    assert lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, 0, 1, 8, 2, 128, 64, 1, 0.125, 0, None,
+                          None) == api.FA_ERR_INVALID  # workspace too small
