@@ -11,6 +11,8 @@ Recipe (one per workload):
   * The block-sparse workload's 128x128 block mask: generator seeded with ``seed + 1000``;
     off-diagonal blocks kept iid with probability 0.25, every diagonal block kept.
   * Grouped-query workloads draw K and V with H_kv heads ([B, H_kv, N, d]); Q and dO keep H.
+  * Decode workloads draw Q [B, H, Nq, d], then the cache K, V [B, H_kv, Nk, d], then (ragged
+    ones) the per-batch cache lengths uniform in [Nk / 2, Nk], from one seeded generator.
 
 The five workloads follow the shapes of the FlashAttention-2 reading notes' kernel benchmark
 (seq 512-16k, hidden 2048, heads of 64/128) and the GPT-style 8k training shape the notes quote.
@@ -129,3 +131,56 @@ def workload_inputs(w: Workload) -> Dict[str, torch.Tensor]:
     if w.sparse_p is not None:
         out["block_mask"] = make_block_mask(w.tiles, w.seed + 1000, w.sparse_p)
     return out
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """A few new query rows per sequence against a KV cache of Nk positions."""
+    name: str
+    B: int
+    H: int
+    h_kv: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+    ragged: bool = False  # per-batch cache lengths in [Nk / 2, Nk] instead of all Nk
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float16 if self.dtype == "fp16" else torch.bfloat16
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def describe(self) -> str:
+        lens = "ragged cache lengths" if self.ragged else "full cache"
+        return (f"{self.name}: decode B={self.B} H={self.H} H_kv={self.h_kv} Nq={self.Nq} "
+                f"Nk={self.Nk} d={self.d} {self.dtype}, {lens}")
+
+
+DECODE_WORKLOADS: Dict[str, DecodeWorkload] = {
+    # one new token per sequence, 16 sequences of 8k cached tokens, 32 query / 8 K/V heads
+    "decode_gqa_d128_kv8k": DecodeWorkload("decode_gqa_d128_kv8k", 16, 32, 8, 1, 8192, 128,
+                                           "bf16", False, 7),
+}
+
+
+def make_decode_inputs(B: int, H: int, h_kv: int, Nq: int, Nk: int, d: int, dtype: torch.dtype,
+                       seed: int, ragged: bool = False) -> Dict[str, torch.Tensor]:
+    """Q, the K/V cache and (ragged) int32 cache lengths, in that order from one generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = {"q": torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(dtype),
+           "k": torch.randn((B, h_kv, Nk, d), generator=g, dtype=torch.float32).to(dtype),
+           "v": torch.randn((B, h_kv, Nk, d), generator=g, dtype=torch.float32).to(dtype)}
+    if ragged:
+        out["kv_len"] = torch.randint(Nk // 2, Nk + 1, (B,), generator=g, dtype=torch.int32)
+    return out
+
+
+def decode_inputs(w: DecodeWorkload) -> Dict[str, torch.Tensor]:
+    return make_decode_inputs(w.B, w.H, w.h_kv, w.Nq, w.Nk, w.d, w.torch_dtype, w.seed, w.ragged)

@@ -205,3 +205,43 @@ def attention_gqa(q, k, v, scale: float, causal: bool = False, block_mask=None, 
         res["dk"] = res["dk"].reshape(B, Hkv, rep, Nk, d).sum(axis=2)
         res["dv"] = res["dv"].reshape(B, Hkv, rep, Nk, d).sum(axis=2)
     return res
+
+
+def decode(q, k, v, scale: float, causal: bool = False, kv_len=None) -> dict:
+    """Attention of a few new query rows against a KV cache, in plain fp64 numpy.
+
+    FlashAttention-2 reading notes, section on the KV cache: in the decode phase each step's
+    query is 1 x d (or a few rows) and attends to the N cached keys.  q [B, H, Nq, d];
+    k, v [B, H_kv, Nk, d] with H_kv dividing H (query head h reads K/V head h // (H / H_kv), as
+    in ``attention_gqa``); batch b uses its first ``kv_len[b]`` cached keys (all Nk when None).
+    With ``causal`` the Nq new rows are the last positions of the sequence: row r is position
+    kv_len - Nq + r and sees keys j <= that position (rows and keys aligned at the end).
+    Per row this is the definition itself: s = scale * K q, P = exp(s - max s) / sum,
+    O = P V, LSE = max s + ln sum exp(s - max s); a row that sees no key gets O = 0 and
+    LSE = -inf.
+    """
+    qa, ka, va = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = qa.shape
+    Hkv, Nk = ka.shape[1], ka.shape[2]
+    if ka.shape != va.shape or ka.shape[0] != B or ka.shape[3] != d or H % Hkv != 0:
+        raise ValueError("q [B, H, Nq, d], k and v [B, H_kv, Nk, d] with H_kv dividing H")
+    lens = np.full(B, Nk, dtype=np.int64) if kv_len is None else \
+        np.asarray(kv_len.detach().cpu().numpy() if hasattr(kv_len, "detach") else kv_len,
+                   dtype=np.int64)
+    rep = H // Hkv
+    o = np.zeros_like(qa)
+    lse = np.full((B, H, Nq), -np.inf)
+    for b in range(B):
+        L = int(min(max(lens[b], 0), Nk))
+        for h in range(H):
+            K, V = ka[b, h // rep, :L], va[b, h // rep, :L]
+            for r in range(Nq):
+                last = L - Nq + r if causal else L - 1  # last key this row sees
+                if last < 0:
+                    continue
+                s = scale * (K[:last + 1] @ qa[b, h, r])
+                m = s.max()
+                p = np.exp(s - m)
+                o[b, h, r] = (p @ V[:last + 1]) / p.sum()
+                lse[b, h, r] = m + np.log(p.sum())
+    return {"o": o, "lse": lse}

@@ -403,3 +403,67 @@ def test_gqa_rejects_heads_that_do_not_divide():
     with pytest.raises(ValueError):
         oracle.attention_gqa(rand((1, 4, 8, 4), 1), rand((1, 3, 8, 4), 2), rand((1, 3, 8, 4), 3),
                              0.5)
+
+
+# ---------------------------------------------------------------- decode against a KV cache
+# FlashAttention-2 reading notes, KV-cache section: a few new query rows against the cache.
+
+def test_decode_with_every_row_new_is_causal_attention():
+    # Nq = Nk = kv_len: the new rows are the whole sequence, so end alignment is the usual
+    # causal mask of the (pinned) three-pass oracle
+    q, k, v = (rand((2, 3, 19, 8), s) for s in (100, 101, 102))
+    a = oracle.decode(q, k, v, 0.3, causal=True)
+    b = oracle.attention(q, k, v, 0.3, True)
+    np.testing.assert_allclose(a["o"], b["o"], atol=1e-13)
+    np.testing.assert_allclose(a["lse"], b["lse"], atol=1e-13)
+
+
+def test_decode_noncausal_ragged_lengths_match_truncated_attention():
+    B, H, Hkv, Nq, Nk, d = 3, 4, 2, 3, 40, 8
+    q = rand((B, H, Nq, d), 103)
+    k, v = rand((B, Hkv, Nk, d), 104), rand((B, Hkv, Nk, d), 105)
+    lens = [40, 17, 1]
+    a = oracle.decode(q, k, v, 0.5, kv_len=lens)
+    for b, L in enumerate(lens):
+        ref = oracle.attention_gqa(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], 0.5)
+        np.testing.assert_allclose(a["o"][b:b + 1], ref["o"], atol=1e-13)
+        np.testing.assert_allclose(a["lse"][b:b + 1], ref["lse"], atol=1e-13)
+
+
+def test_decode_causal_rows_are_the_last_rows_of_a_square_problem():
+    # Nq new rows at the end of a length-L sequence: rows L-Nq .. L-1 of the square causal
+    # problem whose earlier query rows are anything (here zeros)
+    L, Nq, d = 37, 5, 8
+    q, k, v = rand((1, 1, Nq, d), 106), rand((1, 1, L, d), 107), rand((1, 1, L, d), 108)
+    a = oracle.decode(q, k, v, 0.4, causal=True)
+    qfull = np.zeros((L, d))
+    qfull[L - Nq:] = q[0, 0]
+    o, lse = oracle.forward_rows(qfull, k[0, 0], v[0, 0], 0.4, list(range(L - Nq, L)), True)
+    np.testing.assert_allclose(a["o"][0, 0], o, atol=1e-13)
+    np.testing.assert_allclose(a["lse"][0, 0], lse, atol=1e-13)
+
+
+def test_decode_rows_that_see_nothing():
+    q, k, v = rand((2, 1, 4, 4), 109), rand((2, 1, 10, 4), 110), rand((2, 1, 10, 4), 111)
+    a = oracle.decode(q, k, v, 1.0, causal=True, kv_len=[0, 2])
+    assert np.all(a["o"][0] == 0) and np.all(np.isneginf(a["lse"][0]))
+    # batch 1: length 2 with 4 new rows: rows 0, 1 are positions -2, -1 (nothing), rows 2, 3
+    # are positions 0 and 1
+    assert np.all(a["o"][1, 0, :2] == 0) and np.all(np.isneginf(a["lse"][1, 0, :2]))
+    np.testing.assert_allclose(a["o"][1, 0, 2], v[1, 0, 0], atol=1e-15)
+    assert a["lse"][1, 0, 2] == pytest.approx(float(q[1, 0, 2] @ k[1, 0, 0]), abs=1e-14)
+
+
+def test_split_key_ranges_merge_to_the_whole_row():
+    # FlashAttention paper detail, Technique 1: the statistics (and, scaled the same way, the
+    # outputs) of two key ranges combine into those of their concatenation
+    q, k, v = rand((1, 1, 1, 16), 112), rand((1, 1, 300, 16), 113), rand((1, 1, 300, 16), 114)
+    whole = oracle.decode(q, k, v, 0.25)
+    a = oracle.decode(q, k[:, :, :123], v[:, :, :123], 0.25)
+    b = oracle.decode(q, k[:, :, 123:], v[:, :, 123:], 0.25)
+    la, lb = a["lse"][0, 0, 0], b["lse"][0, 0, 0]
+    m, l = recurrence.merge_stats(la, 1.0, lb, 1.0)  # each part's l is e^{LSE - LSE} = 1
+    wa, wb = np.exp(la - m) / l, np.exp(lb - m) / l
+    np.testing.assert_allclose(m + np.log(l), whole["lse"][0, 0, 0], atol=1e-13)
+    np.testing.assert_allclose(wa * a["o"][0, 0, 0] + wb * b["o"][0, 0, 0], whole["o"][0, 0, 0],
+                               atol=1e-13)

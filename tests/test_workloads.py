@@ -57,3 +57,16 @@ def test_grouped_kv_heads_shapes():
     a = make_inputs(2, 6, 40, 8, torch.bfloat16, seed=9, h_kv=2)
     assert a["q"].shape == (2, 6, 40, 8) and a["do"].shape == (2, 6, 40, 8)
     assert a["k"].shape == (2, 2, 40, 8) and a["v"].shape == (2, 2, 40, 8)
+
+
+def test_decode_inputs():
+    from exact_attention_staged_gb300.workloads import DECODE_WORKLOADS, make_decode_inputs
+    w = DECODE_WORKLOADS["decode_gqa_d128_kv8k"]
+    assert (w.B, w.H, w.h_kv, w.Nq, w.Nk, w.d) == (16, 32, 8, 1, 8192, 128)
+    a = make_decode_inputs(3, 4, 2, 2, 64, 8, torch.bfloat16, seed=5, ragged=True)
+    b = make_decode_inputs(3, 4, 2, 2, 64, 8, torch.bfloat16, seed=5, ragged=True)
+    assert a["q"].shape == (3, 4, 2, 8) and a["k"].shape == (3, 2, 64, 8)
+    assert a["kv_len"].dtype == torch.int32 and a["kv_len"].shape == (3,)
+    assert torch.all((a["kv_len"] >= 32) & (a["kv_len"] <= 64))
+    for key in a:
+        assert torch.equal(a[key], b[key])
