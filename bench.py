@@ -34,7 +34,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from exact_attention_staged_gb300.workloads import WORKLOADS, workload_inputs  # noqa: E402
+from exact_attention_staged_gb300.workloads import (DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
+                                                    decode_inputs, workload_inputs)
 
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
@@ -417,17 +418,178 @@ def run_gpu(args, w):
     return 0
 
 
+# ------------------------------------------------------------------------------- decode
+
+def decode_work(w, t):
+    """Algorithmic FLOPs (4 d per visible score: QK and PV) and HBM bytes (the cache rows the
+    sequences use, Q, O and LSE) of one decode step."""
+    lens = t["kv_len"].tolist() if "kv_len" in t else [w.Nk] * w.B
+    fl, cache_rows = 0.0, 0
+    for L in lens:
+        L = max(0, min(int(L), w.Nk))
+        cache_rows += L
+        for r in range(w.Nq):
+            seen = (L - w.Nq + r + 1) if w.causal else L
+            fl += 4.0 * w.H * max(seen, 0) * w.d
+    esz = 2
+    nbytes = 2 * w.h_kv * cache_rows * w.d * esz + 2 * w.B * w.H * w.Nq * w.d * esz + \
+        4 * w.B * w.H * w.Nq
+    return fl, nbytes
+
+
+def run_decode_gpu(args, w):
+    from exact_attention_staged_gb300 import api
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.load()
+    t = decode_inputs(w)
+    q, k, v = (t[x].to(dev) for x in ("q", "k", "v"))
+    lens = t["kv_len"].to(dev) if "kv_len" in t else None
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)
+    nws = api.decode_workspace_bytes(w.B, w.H, w.h_kv, w.Nq, w.Nk, w.d)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.decode(q, k, v, w.scale, w.causal, lens, out=o, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        for s_ in range(args.steps):
+            step()
+            ev[s_ + 1].record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    elapsed_ms = ev[0].elapsed_time(ev[-1])
+    max_ms = dist_max(elapsed_ms, world, dev)
+    fl, nbytes = decode_work(w, t)
+    value = world * fl * args.steps / (max_ms / 1e3) / 1e12
+    step_ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
+    peaks = measured_peaks()
+    gbs = nbytes / (step_ms / 1e3) / 1e9
+    launches = 1 if nws == 0 else 2
+    roofline = {"bound": "hbm", "kernel": "fa_decode_kernel" +
+                ("" if nws == 0 else " + fa_decode_combine_kernel"),
+                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                "algorithmic_bytes": nbytes,
+                "peak_kind": f"HBM copy ({peaks['source']})"}
+
+    # end to end: the cache and the new rows from pinned host memory, O and LSE back
+    hq, hk, hv = (t[x].pin_memory() for x in ("q", "k", "v"))
+    ho = torch.empty_like(hq).pin_memory()
+    hlse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse))
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world, dev)
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error")
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.decode(t["q"], t["k"], t["v"], w.scale, w.causal, t.get("kv_len"))
+        secs = time.perf_counter() - t0
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+               "kind": "oracle", "sample": f"the whole step ({w.B * w.H * w.Nq} rows), fp64 "
+                                           f"numpy, {secs:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "H_kv": w.h_kv, "Nq": w.Nq,
+                   "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "l2": f"cache larger than L2 ({nbytes / 1e6:.0f} MB per step vs "
+                         f"{L2_BYTES / 1e6:.0f} MB L2), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * fl * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_decode_reference(args, w):
+    import oracle
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    t = decode_inputs(w)
+    fl, _ = decode_work(w, t)
+    for _ in range(args.warmup):
+        oracle.decode(t["q"], t["k"], t["v"], w.scale, w.causal, t.get("kv_len"))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(t["q"], t["k"], t["v"], w.scale, w.causal, t.get("kv_len"))
+    secs = time.perf_counter() - t0
+    value = fl * args.steps / secs / 1e12
+    cores = torch.get_num_threads()
+    sample = f"the whole decode step ({w.B * w.H * w.Nq} rows) per step, fp64 numpy oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.describe()},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.workload in DECODE_WORKLOADS:
+        w = DECODE_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            return run_decode_reference(args, w)
+        return run_decode_gpu(args, w)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

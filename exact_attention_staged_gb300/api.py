@@ -38,6 +38,9 @@ SIGNATURES = {
     "fa_bwd_dq": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                             _f, _i, _vp, _vp]),
+    "fa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
+                       _sz, _vp]),
     "fa_sync_status": (_i, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_debug_set_visit_log": (_i, [_vp, _sz]),
@@ -256,6 +259,40 @@ def bwd_gqa(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool =
                           nbytes, B, H, Hkv, N, d, _dtype_code(q), float(scale),
                           int(bool(causal)), mask_ptr, _stream(stream)), "fa_bwd_gqa")
     return dq, dk, dv
+
+
+def decode_workspace_bytes(B: int, H: int, H_kv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_decode_workspace_bytes(B, H, H_kv, Nq, Nk, d))
+
+
+def decode(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_len=None,
+           out=None, lse=None, workspace=None, stream=None):
+    """O, LSE of Nq new rows q [B, H, Nq, d] against the cache k, v [B, H_kv, Nk, d] (fa_decode).
+
+    kv_len: int32 CUDA tensor [B] of valid cache lengths, or None for Nk.
+    """
+    lib = load()
+    B, H, Nq, d = _shape(q)
+    if k.dim() != 4 or k.shape != v.shape or k.shape[0] != B or k.shape[3] != d \
+            or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must be [B, H_kv, Nk, d] with the dtype of q")
+    Hkv, Nk = int(k.shape[1]), int(k.shape[2])
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("lse must be fp32 [B, H, Nq]")
+    if kv_len is not None and (kv_len.dtype != torch.int32 or tuple(kv_len.shape) != (B,)):
+        raise ValueError("kv_len must be int32 [B]")
+    nbytes = decode_workspace_bytes(B, H, Hkv, Nq, Nk, d)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws = None if workspace is None else _dev(workspace, "workspace")
+    _check(lib.fa_decode(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
+                         _dev(lse, "lse"), None if kv_len is None else _dev(kv_len, "kv_len"),
+                         B, H, Hkv, Nq, Nk, d, _dtype_code(q), float(scale), int(bool(causal)),
+                         ws, nbytes, _stream(stream)), "fa_decode")
+    return out, lse
 
 
 def sync_status(stream=None) -> int:

@@ -307,6 +307,33 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
                   stream);
 }
 
+// Decode key ranges: as many per (K/V head, row group) as fit the whole grid into one wave of
+// three 128-thread CTAs per SM on a 152-SM GB300 (a second, partial wave would leave most of the
+// GPU idle while it runs), but no range shorter than 256 keys; ranges are multiples of the
+// kernel's 32-key tile.
+constexpr long kDecodeWaveCtas = 3 * 152;
+struct DecodeSplit {
+    int splits, chunk, row_groups;
+};
+DecodeSplit decode_split(int B, int H, int Hkv, int Nq, int Nk) {
+    const int rows = (H / Hkv) * Nq;
+    const int row_groups = (rows + 15) / 16;
+    const long units = static_cast<long>(B) * Hkv * row_groups;
+    long s = kDecodeWaveCtas / units;
+    const long max_s = (Nk + 255) / 256;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    int chunk = static_cast<int>((Nk + s - 1) / s);
+    chunk = (chunk + 31) / 32 * 32;
+    return {(Nk + chunk - 1) / chunk, chunk, row_groups};
+}
+
+size_t decode_part_bytes(const DecodeSplit &sp, int B, int H, int Nq, int d) {
+    if (sp.splits == 1) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * Nq * sp.splits;
+    return rows * d * sizeof(float) + rows * 2 * sizeof(float);
+}
+
 // Scratch of fa_bwd_noalloc: the D values (one float per query row) of one backward call.
 // Host code must not pass this name to a kernel: on the host it only stands in for the
 // symbol; noalloc_scratch() looks up its device address once per device.
@@ -424,6 +451,58 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
     if (rc != FA_OK) return rc;
     return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, DkvSplit{1, 1}, nullptr, B, H, H, N,
                    d, dtype, scale, causal, block_mask, stream);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int Nq, int Nk, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || check_heads(H, H_kv) != FA_OK) return 0;
+    return decode_part_bytes(decode_split(B, H, H_kv, Nq, Nk), B, H, Nq, d);
+}
+
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+              const int *kv_len, int B, int H, int H_kv, int Nq, int Nk, int d, int dtype,
+              float scale, int causal, void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID;
+    if (static_cast<long long>(B) * H * Nq >= (1ll << 31) ||
+        static_cast<long long>(B) * H_kv * Nk >= (1ll << 31))
+        return FA_ERR_INVALID;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID;
+    if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID;
+    if (check_heads(H, H_kv) != FA_OK) return FA_ERR_INVALID;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    int rc = check_ptrs({q, k, v, o, lse});
+    if (rc != FA_OK) return rc;
+    if (kv_len != nullptr && (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return FA_ERR_INVALID;
+    const DecodeSplit sp = decode_split(B, H, H_kv, Nq, Nk);
+    const size_t need = decode_part_bytes(sp, B, H, Nq, d);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
+        return FA_ERR_INVALID;
+    int dev = 0, *status = nullptr;
+    rc = device_setup(&dev, &status);
+    if (rc != FA_OK) return rc;
+    fa::DecodeParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.kv_len = kv_len;
+    p.part_o = need > 0 ? static_cast<float *>(workspace) : nullptr;
+    p.part_ml = need > 0 ? static_cast<float *>(workspace) +
+                               static_cast<size_t>(B) * H * Nq * sp.splits * d
+                         : nullptr;
+    p.B = B;
+    p.H = H;
+    p.Hkv = H_kv;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.rows = (H / H_kv) * Nq;
+    p.row_groups = sp.row_groups;
+    p.splits = sp.splits;
+    p.chunk = sp.chunk;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal ? 1 : 0;
+    cudaError_t e = fa::launch_decode(p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_sync_status(void *stream) {

@@ -1,0 +1,345 @@
+// fa_decode.cu - decode: a few new query rows per sequence against a KV cache, sm_103a.
+//
+// FlashAttention-2 reading notes, section on the KV cache: in the decode phase each step's
+// query is 1 x d (a few rows here) against the N cached keys, so the product is a matrix-vector
+// one and the kernel is bound by reading K and V from HBM, not by arithmetic.  The work is
+// therefore split over the cache, not over queries: CTA (K/V head, key range, row group) runs
+// the online softmax (running max m and sum l per row, FlashAttention-2 Algorithm 1) over its
+// key range for every query row that reads this K/V head (all query heads of a grouped-query
+// group, times the new rows), reading each cached K/V row once.  Key ranges are merged by the
+// statistic merge of the FlashAttention paper detail, Technique 1 (m = max(m1, m2),
+// l = e^(m1-m) l1 + e^(m2-m) l2, and the outputs weighted the same way).
+//
+// GB300 mapping: no tensor cores (one to sixteen rows per key: 4 to 64 FLOP per 16-bit K/V
+// element pair, far below what would make the MMA pipe the limit); 128 threads per CTA, a few
+// CTAs per SM.  K and V tiles of 32 keys stream through a two-stage cp.async ring into
+// padded shared-memory rows (272 or 144 bytes, so 16-byte reads of 8 consecutive rows hit
+// distinct banks).  Per tile:
+//   A   every warp takes a quarter of d, every lane one key: partial dot products of that key
+//       with all rows (query rows broadcast from shared memory, fp32, pre-scaled by
+//       scale * log2 e);
+//   A2  warp w owns rows w, w+4, ...: sums the four quarters, masks, takes the tile max with
+//       shuffles, P = 2^(s - m), l = alpha l + sum P;
+//   B   every thread owns two output columns of some rows: O = alpha O + P V.
+// With one key range the CTA writes O and LSE; otherwise it writes (m, l, unnormalised O) and
+// fa_decode_combine_kernel merges the ranges in order (deterministic).
+#include "fa_internal.h"
+
+#include <cmath>
+#include <type_traits>
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kKeys = 32;     // keys per shared-memory tile
+constexpr int kStages = 3;    // K/V tiles in the cp.async ring (two in flight while one is used)
+
+template <int D, int RPC>
+struct DecLayout {
+    static constexpr int kRowBytes = D * 2 + 16;  // padded 16-bit K or V row
+    static constexpr int kTileBytes = kKeys * kRowBytes;
+    static constexpr int kQOff = 0;                                 // float [RPC][D]
+    static constexpr int kKOff = kQOff + RPC * D * 4;               // kStages tiles
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;      // kStages tiles
+    static constexpr int kPartOff = kVOff + kStages * kTileBytes;   // float [4][RPC][32]
+    static constexpr int kPOff = kPartOff + 4 * RPC * kKeys * 4;    // float [RPC][32]
+    static constexpr int kStatOff = kPOff + RPC * kKeys * 4;        // alpha, m, l [RPC] each
+    static constexpr int kBytes = kStatOff + 3 * RPC * 4;
+};
+
+template <bool BF16>
+using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// RPC: query rows per CTA (1, 2, 4, 8 or 16), the smallest that holds a K/V head's rows.
+template <int D, bool BF16, int RPC>
+__global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams p) {
+    using L = DecLayout<D, RPC>;
+    using T = elem_t<BF16>;
+    constexpr int kPairs = D / 2;                 // column pairs of O
+    constexpr int kRB = kThreads / kPairs;        // row sets in phase B (2 for d=128, 4 for 64)
+    constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in phase B
+    constexpr int kQuarter = D / 4;               // columns per warp in phase A
+    constexpr int kChunks = D * 2 / 16;           // 16-byte chunks per K/V row
+    constexpr int kRowsA2 = (RPC + 3) / 4;        // rows per warp in phase A2
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *qs = reinterpret_cast<float *>(smem + L::kQOff);
+    float *part = reinterpret_cast<float *>(smem + L::kPartOff);
+    float *ps = reinterpret_cast<float *>(smem + L::kPOff);
+    float *alpha_s = reinterpret_cast<float *>(smem + L::kStatOff);
+    float *m_s = alpha_s + RPC;
+    float *l_s = m_s + RPC;
+
+    // block order: row group fastest, then key range, then K/V head (b * H_kv + g)
+    unsigned bid = blockIdx.x;
+    const int rg = static_cast<int>(bid % static_cast<unsigned>(p.row_groups));
+    bid /= static_cast<unsigned>(p.row_groups);
+    const int split = static_cast<int>(bid % static_cast<unsigned>(p.splits));
+    const int kvh = static_cast<int>(bid / static_cast<unsigned>(p.splits));
+    const int b = kvh / p.Hkv;
+    const int r0 = rg * RPC;
+    const int nrows = min(RPC, p.rows - r0);
+    int len = p.kv_len != nullptr ? p.kv_len[b] : p.Nk;
+    len = max(0, min(len, p.Nk));
+    const int k_begin = split * p.chunk;
+    const int k_end = min(k_begin + p.chunk, len);
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // CTA row r is group row r0 + r: query head kvh * rep + (r0 + r) / Nq, new row (r0 + r) % Nq,
+    // i.e. global row ((b * H + h) * Nq + i) = kvh * rows + r0 + r
+    const long grow0 = static_cast<long>(kvh) * p.rows + r0;
+    const T *kbase = reinterpret_cast<const T *>(p.k) + static_cast<size_t>(kvh) * p.Nk * D;
+    const T *vbase = reinterpret_cast<const T *>(p.v) + static_cast<size_t>(kvh) * p.Nk * D;
+
+    auto load_tile = [&](int t) {  // always commits a group, empty past the last tile
+        if (t < ntiles) {
+            const int key0 = k_begin + kKeys * t;
+            const int stage = t % kStages;
+#pragma unroll
+            for (int i = tid; i < 2 * kKeys * kChunks; i += kThreads) {
+                const int kv = i / (kKeys * kChunks);
+                const int rem = i - kv * kKeys * kChunks;
+                const int row = rem / kChunks, ch = rem - row * kChunks;
+                const int key = key0 + row;
+                const bool in = key < k_end;
+                const T *src =
+                    (kv ? vbase : kbase) + static_cast<size_t>(in ? key : 0) * D + ch * 8;
+                uint8_t *dst = smem + (kv ? L::kVOff : L::kKOff) + stage * L::kTileBytes +
+                               row * L::kRowBytes + ch * 16;
+                cp_async_16(dst, src, in);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int t = 0; t < kStages - 1; ++t) load_tile(t);
+
+    const T *qrows = reinterpret_cast<const T *>(p.q) + static_cast<size_t>(grow0) * D;
+    for (int i = tid; i < RPC * D; i += kThreads)
+        qs[i] = i < nrows * D ? static_cast<float>(qrows[i]) * p.scale_log2 : 0.f;
+
+    float m_run[kRowsA2], l_run[kRowsA2];
+#pragma unroll
+    for (int i = 0; i < kRowsA2; ++i) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.f;
+    }
+    const int cp = tid % kPairs, rs = tid / kPairs;
+    float acc[kRowsB][2];
+#pragma unroll
+    for (int j = 0; j < kRowsB; ++j) acc[j][0] = acc[j][1] = 0.f;
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int stage = t % kStages;
+        cp_async_wait_group<kStages - 2>();  // tile t has landed (this thread's part)
+        __syncthreads();  // ... everyone's part; and everyone is done with tile t - 1
+        load_tile(t + kStages - 1);  // into the stage tile t - 1 used
+
+        {  // A: partial dots of key `lane` over columns [warp * D/4, (warp + 1) * D/4)
+            const uint8_t *krow =
+                smem + L::kKOff + stage * L::kTileBytes + lane * L::kRowBytes + warp * kQuarter * 2;
+            float dot[RPC];
+#pragma unroll
+            for (int r = 0; r < RPC; ++r) dot[r] = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < kQuarter / 8; ++c8) {
+                const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8 * 16);
+                const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+                float kf[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack2<BF16>(w4[e]);
+                    kf[2 * e] = f.x;
+                    kf[2 * e + 1] = f.y;
+                }
+#pragma unroll
+                for (int r = 0; r < RPC; ++r) {  // rows past nrows hold zeros
+                    const float4 *qv =
+                        reinterpret_cast<const float4 *>(qs + r * D + warp * kQuarter + c8 * 8);
+                    const float4 a = qv[0], c = qv[1];
+                    float d = dot[r];
+                    d = fmaf(a.x, kf[0], d);
+                    d = fmaf(a.y, kf[1], d);
+                    d = fmaf(a.z, kf[2], d);
+                    d = fmaf(a.w, kf[3], d);
+                    d = fmaf(c.x, kf[4], d);
+                    d = fmaf(c.y, kf[5], d);
+                    d = fmaf(c.z, kf[6], d);
+                    d = fmaf(c.w, kf[7], d);
+                    dot[r] = d;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPC; ++r) part[(warp * RPC + r) * kKeys + lane] = dot[r];
+        }
+        __syncthreads();
+        {  // A2: warp w owns rows w, w + 4, w + 8, w + 12
+            const int key = k_begin + kKeys * t + lane;
+#pragma unroll
+            for (int i = 0; i < kRowsA2; ++i) {
+                const int r = warp + 4 * i;
+                if (r < nrows) {
+                    const int gr = r0 + r;
+                    const int last = p.causal ? len - p.Nq + gr % p.Nq : len - 1;
+                    float s = part[r * kKeys + lane] + part[(RPC + r) * kKeys + lane] +
+                              part[(2 * RPC + r) * kKeys + lane] +
+                              part[(3 * RPC + r) * kKeys + lane];
+                    if (key >= k_end || key > last) s = -INFINITY;
+                    const float m_new = fmaxf(m_run[i], warp_max(s));
+                    float alpha = 1.f, pr = 0.f;
+                    if (m_new != -INFINITY) {  // ex2(-inf) = 0 covers masked keys, first tile
+                        alpha = ex2(m_run[i] - m_new);
+                        pr = ex2(s - m_new);
+                    }
+                    l_run[i] = l_run[i] * alpha + warp_sum(pr);
+                    m_run[i] = m_new;
+                    ps[r * kKeys + lane] = pr;
+                    if (lane == 0) alpha_s[r] = alpha;
+                }
+            }
+        }
+        __syncthreads();
+        {  // B: O = alpha O + P V for this thread's two columns
+            const uint8_t *vcol = smem + L::kVOff + stage * L::kTileBytes + cp * 4;
+#pragma unroll
+            for (int j = 0; j < kRowsB; ++j) {
+                const int r = rs + kRB * j;
+                if (r < nrows) {
+                    const float a = alpha_s[r];
+                    acc[j][0] *= a;
+                    acc[j][1] *= a;
+                }
+            }
+            if (rs < nrows) {
+#pragma unroll 8
+                for (int key = 0; key < kKeys; ++key) {
+                    const float2 vv = unpack2<BF16>(
+                        *reinterpret_cast<const uint32_t *>(vcol + key * L::kRowBytes));
+#pragma unroll
+                    for (int j = 0; j < kRowsB; ++j) {
+                        const int r = rs + kRB * j;
+                        if (RPC % kRB == 0 || r < RPC) {  // compile-time for whole row sets
+                            const float pp = r < nrows ? ps[r * kKeys + key] : 0.f;
+                            acc[j][0] = fmaf(pp, vv.x, acc[j][0]);
+                            acc[j][1] = fmaf(pp, vv.y, acc[j][1]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait_group<0>();  // no copy may still target shared memory at exit
+
+#pragma unroll
+    for (int i = 0; i < kRowsA2; ++i) {
+        const int r = warp + 4 * i;
+        if (r < nrows && lane == 0) {
+            m_s[r] = m_run[i];
+            l_s[r] = l_run[i];
+        }
+    }
+    __syncthreads();
+    const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
+#pragma unroll
+    for (int j = 0; j < kRowsB; ++j) {
+        const int r = rs + kRB * j;
+        if (r >= nrows) continue;
+        const long grow = grow0 + r;
+        const float m = m_s[r], l = l_s[r];
+        if (p.splits == 1) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.o) + grow * D)[cp] =
+                pack2<BF16>(acc[j][0] * inv, acc[j][1] * inv);
+            if (cp == 0)
+                p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        } else {
+            const long prow = static_cast<long>(split) * total_rows + grow;
+            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = make_float2(acc[j][0], acc[j][1]);
+            if (cp == 0) reinterpret_cast<float2 *>(p.part_ml)[prow] = make_float2(m, l);
+        }
+    }
+}
+
+// Merge of the key ranges of every row, in range order: M = max m_s, w_s = 2^(m_s - M),
+// l = sum w_s l_s, O = sum w_s O_s / l, LSE = (M + log2 l) ln 2.  One warp per row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
+    using T = elem_t<BF16>;
+    constexpr int kCols = D / 32;
+    const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
+    const long row = static_cast<long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= total_rows) return;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, ml[static_cast<long>(s) * total_rows + row].x);
+    float lsum = 0.f, acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+        const long prow = static_cast<long>(s) * total_rows + row;
+        const float2 st = ml[prow];
+        if (st.x == -INFINITY) continue;  // an empty range (also covers M = -inf)
+        const float w = ex2(st.x - M);
+        lsum = fmaf(w, st.y, lsum);
+        const float *src = p.part_o + prow * D + lane * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, src[c], acc[c]);
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    T *dst = reinterpret_cast<T *>(p.o) + row * D + lane * kCols;
+#pragma unroll
+    for (int c = 0; c < kCols; c += 2)
+        reinterpret_cast<uint32_t *>(dst + c)[0] = pack2<BF16>(acc[c] * inv, acc[c + 1] * inv);
+    if (lane == 0) p.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <int D, bool BF16, int RPC>
+cudaError_t launch_decode_rpc(const DecodeParams &p, cudaStream_t stream) {
+    using L = DecLayout<D, RPC>;
+    auto kern = fa_decode_kernel<D, BF16, RPC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kBytes);
+    if (e != cudaSuccess) return e;
+    const long grid = static_cast<long>(p.B) * p.Hkv * p.splits * p.row_groups;
+    kern<<<static_cast<unsigned>(grid), kThreads, L::kBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
+    const int rpc = p.rows >= 16 ? 16 : p.rows;  // rows per CTA: the row group size
+    cudaError_t e;
+    if (rpc <= 1) e = launch_decode_rpc<D, BF16, 1>(p, stream);
+    else if (rpc <= 2) e = launch_decode_rpc<D, BF16, 2>(p, stream);
+    else if (rpc <= 4) e = launch_decode_rpc<D, BF16, 4>(p, stream);
+    else if (rpc <= 8) e = launch_decode_rpc<D, BF16, 8>(p, stream);
+    else e = launch_decode_rpc<D, BF16, 16>(p, stream);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    const long rows = static_cast<long>(p.B) * p.H * p.Nq;
+    fa_decode_combine_kernel<D, BF16>
+        <<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_decode_t<64, true>(p, stream)
+                             : launch_decode_t<64, false>(p, stream);
+    return bf16 ? launch_decode_t<128, true>(p, stream) : launch_decode_t<128, false>(p, stream);
+}
+
+}  // namespace fa

@@ -68,6 +68,23 @@ struct BwdParams {
     Ctl ctl;
 };
 
+// Decode: a few new query rows per sequence against a KV cache (see fa_decode.cu).
+struct DecodeParams {
+    const void *q;            // [B,H,Nq,d]
+    const void *k, *v;        // [B,H_kv,Nk,d] cache
+    void *o;                  // [B,H,Nq,d]
+    float *lse;               // [B,H,Nq]
+    const int *kv_len;        // [B] cache lengths, or nullptr for Nk
+    float *part_o;            // splits > 1: [splits][B*H*Nq][d] unnormalised partial outputs
+    float *part_ml;           //             [splits][B*H*Nq][2] running max (log2) and sum
+    int B, H, Hkv, Nq, Nk;
+    int rows;                 // (H / H_kv) * Nq: query rows that share one K/V head
+    int row_groups;           // ceil(rows / 16): CTAs per K/V head and key range
+    int splits, chunk;        // key ranges [s * chunk, (s + 1) * chunk), chunk a multiple of 32
+    float scale_log2;         // scale * log2(e)
+    int causal;               // new rows end-aligned with the cache
+};
+
 struct Maps {
     CUtensorMap q, k, v, dout;
 };
@@ -80,6 +97,7 @@ cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf
                             cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
                           cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int splits,
                                     long kv_elems, bool bf16, cudaStream_t stream);
 

@@ -146,6 +146,19 @@ __device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gsrc, boo
                  "l"(gsrc), "r"(valid ? 4 : 0)
                  : "memory");
 }
+// 16-byte cp.async through L2 only (streamed data); valid == false writes 16 zero bytes.
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Arrive on `bar` (without raising its expected count) once this thread's cp.async are done.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))

@@ -171,6 +171,28 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    int dtype, float scale, int causal, const uint8_t *block_mask, void *stream);
 
 /*
+ * Decode: a few new query rows per sequence against a KV cache.  FlashAttention-2 reading
+ * notes, section on the KV cache (a 1 x d query per generated token against the N cached keys);
+ * key ranges of the cache are processed by separate CTAs and merged with the statistic merge of
+ * the FlashAttention paper detail, Technique 1.  The kernel is bound by reading K and V.
+ *   q, o    : [B,H,Nq,d] (device), Nq >= 1 new rows per sequence;  lse : [B,H,Nq] fp32.
+ *   k, v    : [B,H_kv,Nk,d] cache (device), Nk = its capacity; H_kv divides H and query head h
+ *             reads K/V head h / (H / H_kv) (as fa_fwd_gqa).
+ *   kv_len  : device int32 [B], the number of valid cached positions of each sequence (values
+ *             are clamped to [0, Nk]), or NULL for Nk everywhere.
+ *   causal  : 0: every new row sees all kv_len[b] keys.  != 0: the new rows are the last Nq
+ *             positions of the sequence, row r is position kv_len[b] - Nq + r and sees keys
+ *             j <= that position.  A row that sees no key gets O = 0 and LSE = -inf.
+ *   workspace, workspace_bytes : device scratch of fa_decode_workspace_bytes() bytes,
+ *             16-byte aligned (may be NULL when that is 0): the per-range partial results.
+ * Errors as fa_fwd; B*H*Nq and B*H_kv*Nk must be below 2^31.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int Nq, int Nk, int d);
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+              const int *kv_len, int B, int H, int H_kv, int Nq, int Nk, int d, int dtype,
+              float scale, int causal, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a pipeline wait and returned early; its outputs
  * are undefined) or FA_ERR_CUDA (the stream reported an error).

@@ -112,3 +112,24 @@ def test_gqa_workspace_and_validation(lib):
                               0.125, 0, None, None) == api.FA_ERR_INVALID
     assert lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, p, 0, 1, 8, 2, 128, 64, 1, 0.125, 0, None,
                           None) == api.FA_ERR_INVALID  # workspace too small
+
+
+def test_decode_workspace_and_validation(lib):
+    p = ctypes.c_void_p(16)
+    # 16 sequences x 8 K/V heads at 8k: 128 CTAs per key range, 3 ranges (of 2752 keys) fill
+    # one wave of 456 CTAs
+    rows = 16 * 32 * 1
+    assert api.decode_workspace_bytes(16, 32, 8, 1, 8192, 128) == 3 * rows * (128 + 2) * 4
+    # 256 keys or fewer: a single range, no scratch
+    assert api.decode_workspace_bytes(2, 4, 4, 1, 200, 64) == 0
+    assert lib.fa_decode_workspace_bytes(1, 6, 4, 1, 100, 64) == 0  # 4 does not divide 6
+
+    def dec(q=p, kv_len=None, B=1, H=4, Hkv=2, Nq=1, Nk=128, d=64, ws=None, wsb=0):
+        return lib.fa_decode(q, p, p, p, p, kv_len, B, H, Hkv, Nq, Nk, d, 1, 0.125, 0, ws, wsb,
+                             None)
+    assert dec(q=None) == api.FA_ERR_INVALID
+    assert dec(Nq=0) == api.FA_ERR_INVALID
+    assert dec(Hkv=3) == api.FA_ERR_INVALID
+    assert dec(d=80) == api.FA_ERR_UNSUPPORTED
+    assert dec(kv_len=ctypes.c_void_p(18)) == api.FA_ERR_INVALID  # misaligned lengths
+    assert dec(Nk=4096) == api.FA_ERR_INVALID  # several key ranges but no workspace
