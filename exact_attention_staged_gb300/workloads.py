@@ -11,6 +11,9 @@ Recipe (one per workload):
   * The block-sparse workload's 128x128 block mask: generator seeded with ``seed + 1000``;
     off-diagonal blocks kept iid with probability 0.25, every diagonal block kept.
   * Grouped-query workloads draw K and V with H_kv heads ([B, H_kv, N, d]); Q and dO keep H.
+  * FP8 workloads draw Q, K, V as above in fp32, then quantise each tensor to e4m3 with one
+    scale: descale = amax / 448, code = e4m3(clamp(x / descale, -448, 448)) (round to nearest);
+    the value a code stands for is e4m3(code) * descale.
   * Decode workloads draw Q [B, H, Nq, d], then the cache K, V [B, H_kv, Nk, d], then (ragged
     ones) the per-batch cache lengths uniform in [Nk / 2, Nk], from one seeded generator.
 
@@ -89,6 +92,12 @@ WORKLOADS: Dict[str, Workload] = {
 ORDER = ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k", "gpt_causal_d128_n8k",
          "blocksparse_d64_n16k"]
 EXTENSIONS = ["gqa_causal_d128_n8k"]
+
+# e4m3 forward workloads: the GPT-style 8k shape with Q, K, V quantised per tensor
+FP8_WORKLOADS: Dict[str, Workload] = {
+    "fp8_causal_d128_n8k": Workload("fp8_causal_d128_n8k", 1, 32, 8192, 128, "e4m3", True, 8,
+                                    qk_mult=2.0, backward=False),
+}
 
 
 def make_inputs(B: int, H: int, N: int, d: int, dtype: torch.dtype, seed: int,
@@ -184,3 +193,30 @@ def make_decode_inputs(B: int, H: int, h_kv: int, Nq: int, Nk: int, d: int, dtyp
 
 def decode_inputs(w: DecodeWorkload) -> Dict[str, torch.Tensor]:
     return make_decode_inputs(w.B, w.H, w.h_kv, w.Nq, w.Nk, w.d, w.torch_dtype, w.seed, w.ragged)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """One-scale e4m3 quantisation of an fp32 tensor: (uint8 codes, descale as a float)."""
+    amax = float(x.abs().max())
+    descale = amax / 448.0 if amax > 0 else 1.0
+    codes = (x / descale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), descale
+
+
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int, qk_mult: float = 1.0,
+                    h_kv: Optional[int] = None) -> Dict[str, object]:
+    """Q, K, V drawn as in make_inputs (fp32, same order), each quantised to e4m3 codes."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    kv_shape = (B, H if h_kv is None else h_kv, N, d)
+    q = torch.randn((B, H, N, d), generator=g, dtype=torch.float32) * qk_mult
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32) * qk_mult
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    out: Dict[str, object] = {}
+    for name, x in (("q", q), ("k", k), ("v", v)):
+        out[name], out["descale_" + name] = quantize_e4m3(x)
+    return out
+
+
+def fp8_workload_inputs(w: Workload) -> Dict[str, object]:
+    return make_fp8_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, w.h_kv)

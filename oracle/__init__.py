@@ -245,3 +245,30 @@ def decode(q, k, v, scale: float, causal: bool = False, kv_len=None) -> dict:
                 o[b, h, r] = (p @ V[:last + 1]) / p.sum()
                 lse[b, h, r] = m + np.log(p.sum())
     return {"o": o, "lse": lse}
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Values of e4m3 bytes (OCP 8-bit floating point, E4M3: 1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal, 2^-6 * m / 8; exponent 15 with mantissa 7
+    is NaN; no infinities; largest finite 448)."""
+    c = np.asarray(codes.detach().cpu().numpy() if hasattr(codes, "detach") else codes,
+                   dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def attention_fp8(q, k, v, scale: float, descale_q: float, descale_k: float,
+                  descale_v: float, causal: bool = False, block_mask=None,
+                  block: int = 128) -> dict:
+    """Forward of attention on e4m3 inputs: q [B, H, N, d], k, v [B, H_kv, N, d] as e4m3
+    codes, each tensor standing for code value * its descale.  The attention itself is the
+    plain definition (``attention_gqa``) on those values in fp64; the e4m3 format only decides
+    which values the inputs are."""
+    qa = e4m3_to_f64(q) * descale_q
+    ka = e4m3_to_f64(k) * descale_k
+    va = e4m3_to_f64(v) * descale_v
+    return attention_gqa(qa, ka, va, scale, causal, block_mask, block)

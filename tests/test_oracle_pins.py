@@ -467,3 +467,37 @@ def test_split_key_ranges_merge_to_the_whole_row():
     np.testing.assert_allclose(m + np.log(l), whole["lse"][0, 0, 0], atol=1e-13)
     np.testing.assert_allclose(wa * a["o"][0, 0, 0] + wb * b["o"][0, 0, 0], whole["o"][0, 0, 0],
                                atol=1e-13)
+
+
+
+# ---------------------------------------------------------------- e4m3 inputs
+
+def test_e4m3_decoder_matches_the_format_and_torch():
+    # values fixed by the format: bias 7, 3 mantissa bits, subnormals below 2^-6, max 448
+    fixed = {0x00: 0.0, 0x80: -0.0, 0x38: 1.0, 0x7E: 448.0, 0xFE: -448.0, 0x08: 2.0 ** -6,
+             0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x40: 2.0, 0x3C: 1.5, 0x30: 0.5}
+    got = oracle.e4m3_to_f64(np.array(list(fixed), dtype=np.uint8))
+    np.testing.assert_array_equal(got, np.array(list(fixed.values())))
+    assert np.isnan(oracle.e4m3_to_f64(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    # every code against torch's float8_e4m3fn conversion (a library routine)
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = oracle.e4m3_to_f64(codes)
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(mine[ok], ref[ok])
+
+
+def test_fp8_attention_is_attention_of_the_decoded_values():
+    from exact_attention_staged_gb300.workloads import make_fp8_inputs
+    t = make_fp8_inputs(1, 4, 40, 8, seed=12, h_kv=2)
+    a = oracle.attention_fp8(t["q"], t["k"], t["v"], 0.3, t["descale_q"], t["descale_k"],
+                             t["descale_v"], causal=True)
+    # decode through torch instead, then the (pinned) grouped-query oracle
+    dec = {x: t[x].view(torch.float8_e4m3fn).to(torch.float64) * t["descale_" + x]
+           for x in ("q", "k", "v")}
+    b = oracle.attention_gqa(dec["q"], dec["k"], dec["v"], 0.3, True)
+    np.testing.assert_array_equal(a["o"], b["o"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    for x in ("q", "k", "v"):  # the quantisation leaves every code finite
+        assert not np.isnan(oracle.e4m3_to_f64(t[x])).any()
