@@ -34,8 +34,9 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from exact_attention_staged_gb300.workloads import (DECODE_WORKLOADS, WORKLOADS,  # noqa: E402
-                                                    decode_inputs, workload_inputs)
+from exact_attention_staged_gb300.workloads import (DECODE_WORKLOADS, FP8_WORKLOADS,  # noqa: E402
+                                                    WORKLOADS, decode_inputs,
+                                                    fp8_workload_inputs, workload_inputs)
 
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
@@ -544,6 +545,99 @@ def run_decode_gpu(args, w):
     return 0
 
 
+# ------------------------------------------------------------------------------- e4m3 forward
+
+def run_fp8_gpu(args, w):
+    """The e4m3 forward (V transpose pre-pass + forward kernel, one fa_fwd_fp8 call per step)."""
+    from exact_attention_staged_gb300 import api
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.load()
+    t = fp8_workload_inputs(w)
+    q, k, v = (t[x].to(dev) for x in ("q", "k", "v"))
+    dsc = (t["descale_q"], t["descale_k"], t["descale_v"])
+    o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    ws = torch.empty(api.fp8_workspace_bytes(w.B, w.kv_heads, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.fwd_fp8(q, k, v, *dsc, w.scale, w.causal, out=o, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        for s_ in range(args.steps):
+            step()
+            ev[s_ + 1].record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(world)
+    max_ms = dist_max(ev[0].elapsed_time(ev[-1]), world, dev)
+    if api.sync_status() != 0:
+        raise RuntimeError("device status reported an error in the timed region")
+    fl = flops(w.B, w.H, w.N, w.d, w.causal)["fa_fwd_kernel"]
+    value = world * fl * args.steps / (max_ms / 1e3) / 1e12
+    peaks = measured_peaks()
+    peak = 2.0 * peaks["bf16_tflops"]  # e4m3 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
+    step_ms = max_ms / args.steps
+    hq, hk, hv = (t[x].pin_memory() for x in ("q", "k", "v"))
+    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world, dev)
+    if rank != 0:
+        return 0
+    achieved = fl / (step_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "passes": "fwd",
+                   "l2": "inputs larger than L2 (3 x 33.5 MB codes + 67 MB output), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "fa_fp8_transpose_v_kernel + fa_fwd_fp8_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"e4m3 dense = 2 x bf16 dense burst ({peaks['source']})"},
+        "cpu_baseline": None,
+        "e2e": {"value": world * fl * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(x.numel() for x in (hq, hk, hv)),
+                "d2h_bytes_per_step": ho.numel() * 2 + hlse.numel() * 4, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_decode_reference(args, w):
     import oracle
     world, rank, _ = dist_setup()
@@ -580,11 +674,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(FP8_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.workload in FP8_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the e4m3 workload has no "
+                              "oracle timing arm; its parity runs in tests/test_fp8_gpu.py"}))
+            return 0
+        return run_fp8_gpu(args, FP8_WORKLOADS[args.workload])
     if args.workload in DECODE_WORKLOADS:
         w = DECODE_WORKLOADS[args.workload]
         if args.impl == "reference":

@@ -26,6 +26,9 @@ SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
     "fa_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "fa_fwd_fp8_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _f, _f, _i, _vp,
+                        _vp, _sz, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i,
                     _f, _i, _vp, _vp]),
@@ -228,6 +231,39 @@ def fwd_gqa(q, k, v, scale: Optional[float] = None, causal: bool = False, block_
     _check(lib.fa_fwd_gqa(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
                           _dev(lse, "lse"), B, H, Hkv, N, d, _dtype_code(q), float(scale),
                           int(bool(causal)), mask_ptr, _stream(stream)), "fa_fwd_gqa")
+    return out, lse
+
+
+def fp8_workspace_bytes(B: int, H_kv: int, N: int, d: int) -> int:
+    return int(load().fa_fwd_fp8_workspace_bytes(B, H_kv, N, d))
+
+
+def fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
+            scale: Optional[float] = None, causal: bool = False, block_mask=None, out=None,
+            lse=None, workspace=None, stream=None):
+    """O (bf16), LSE of attention on e4m3 codes (uint8 tensors) with per-tensor scales
+    (fa_fwd_fp8): q [B, H, N, d], k, v [B, H_kv, N, d]."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.uint8:
+            raise TypeError(f"{name} must hold e4m3 codes as torch.uint8")
+    if k.dim() != 4 or k.shape != v.shape or k.shape[0] != B or k.shape[2:] != q.shape[2:]:
+        raise ValueError("k and v must be [B, H_kv, N, d]")
+    Hkv = int(k.shape[1])
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = fp8_workspace_bytes(B, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_fwd_fp8(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out"),
+                          _dev(lse, "lse"), B, H, Hkv, N, d, float(scale), float(descale_q),
+                          float(descale_k), float(descale_v), int(bool(causal)), mask_ptr,
+                          _dev(workspace, "workspace"),
+                          workspace.numel() * workspace.element_size(), _stream(stream)),
+           "fa_fwd_fp8")
     return out, lse
 
 

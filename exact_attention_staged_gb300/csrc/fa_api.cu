@@ -106,6 +106,22 @@ int make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int dtype) 
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D byte tensor (e4m3 codes): dims x (contiguous), y, z; box box_x bytes x box_y rows with
+// the swizzle that matches box_x (128 or 64 bytes).
+int make_map_bytes(CUtensorMap *m, const void *base, long x, long y, long z, int box_x,
+                   int box_y) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(x), static_cast<cuuint64_t>(y),
+                          static_cast<cuuint64_t>(z)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(x), static_cast<cuuint64_t>(x * y)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          box_x == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 
 int check_heads(int H, int Hkv) {
@@ -451,6 +467,56 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
     if (rc != FA_OK) return rc;
     return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, DkvSplit{1, 1}, nullptr, B, H, H, N,
                    d, dtype, scale, causal, block_mask, stream);
+}
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d) {
+    if (B < 1 || H_kv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    const size_t np = (static_cast<size_t>(N) + 15) / 16 * 16;
+    return round256(static_cast<size_t>(B) * H_kv * d * np);
+}
+
+int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int H_kv, int N, int d, float scale, float descale_q, float descale_k,
+               float descale_v, int causal, const uint8_t *block_mask, void *workspace,
+               size_t workspace_bytes, void *stream) {
+    int rc = check_shape(B, H, N, d, FA_BF16, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_heads(H, H_kv);
+    if (rc != FA_OK) return rc;
+    for (float x : {descale_q, descale_k, descale_v})
+        if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_INVALID;
+    rc = check_ptrs({q, k, v, o, lse, workspace});
+    if (rc != FA_OK) return rc;
+    if (workspace_bytes < fa_fwd_fp8_workspace_bytes(B, H_kv, N, d)) return FA_ERR_INVALID;
+    int dev = 0, *status = nullptr;
+    rc = device_setup(&dev, &status);
+    if (rc != FA_OK) return rc;
+    const int Np = (N + 15) / 16 * 16;
+    uint8_t *vt = static_cast<uint8_t *>(workspace);
+    fa::Fp8Maps maps;
+    if (make_map_bytes(&maps.q, q, d, N, static_cast<long>(B) * H, d, fa::kTile) ||
+        make_map_bytes(&maps.k, k, d, N, static_cast<long>(B) * H_kv, d, fa::kTile) ||
+        make_map_bytes(&maps.vt, vt, Np, d, static_cast<long>(B) * H_kv, fa::kTile, d))
+        return FA_ERR_CUDA;
+    fa::Fp8FwdParams p;
+    p.o = o;
+    p.lse = lse;
+    p.mask = block_mask;
+    p.BH = B * H;
+    p.N = N;
+    p.T = tiles_of(N);
+    p.num_pairs = (p.T + 1) / 2;
+    p.rep = H / H_kv;
+    p.head_group = head_group(p.BH, N, d, 1.0 / p.rep);  // K and V^T: d bytes per row each
+    p.scale_log2 = scale * descale_q * descale_k * 1.4426950408889634f;
+    p.descale_v = descale_v;
+    p.causal = causal ? 1 : 0;
+    if (make_ctl(status, p.BH, p.T, &p.ctl) != FA_OK) return FA_ERR_INVALID;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fa::launch_fp8_transpose_v(static_cast<const uint8_t *>(v), vt, B * H_kv, N,
+                                               Np, d, st);
+    if (e == cudaSuccess) e = fa::launch_fwd_fp8(maps, p, d, st);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int H_kv, int Nq, int Nk, int d) {

@@ -68,6 +68,23 @@ struct BwdParams {
     Ctl ctl;
 };
 
+// Forward on e4m3 inputs (see fa_fwd_fp8.cu): the FwdParams fields plus the value scales.
+struct Fp8FwdParams {
+    void *o;                  // [B,H,N,d] bf16 output
+    float *lse;               // [B,H,N]
+    const uint8_t *mask;      // [T][T] or nullptr
+    int BH, N, T, num_pairs, head_group, rep;
+    float scale_log2;         // softmax scale * descale_q * descale_k * log2(e)
+    float descale_v;          // value of one V unit
+    int causal;
+    Ctl ctl;
+};
+
+struct Fp8Maps {
+    CUtensorMap q, k;         // [B*H or B*H_kv, N, d] bytes, boxes d x 128 rows
+    CUtensorMap vt;           // [B*H_kv, d, Np] bytes (V transposed), boxes 128 keys x d rows
+};
+
 // Decode: a few new query rows per sequence against a KV cache (see fa_decode.cu).
 struct DecodeParams {
     const void *q;            // [B,H,Nq,d]
@@ -98,6 +115,10 @@ cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
                           cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream);
+cudaError_t launch_fp8_transpose_v(const uint8_t *v, uint8_t *vt, int BHkv, int N, int Np, int d,
+                                   cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Fp8Maps &maps, const Fp8FwdParams &p, int d,
+                           cudaStream_t stream);
 cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int splits,
                                     long kv_elems, bool bf16, cudaStream_t stream);
 

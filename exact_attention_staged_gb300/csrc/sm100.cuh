@@ -224,6 +224,14 @@ __device__ __forceinline__ SDesc sdesc_make(uint32_t saddr, uint32_t lbo_bytes, 
     d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
     return d;
 }
+// As sdesc_make with the 64-byte swizzle (layout type 4): rows of 64 bytes, 8-row atoms of 512.
+__device__ __forceinline__ SDesc sdesc_make_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                                 uint32_t sbo_bytes) {
+    SDesc d;
+    d.lo = ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+    d.hi = ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+    return d;
+}
 __device__ __forceinline__ SDesc sdesc_add(SDesc d, uint32_t byte_offset) {
     d.lo += byte_offset >> 4;
     return d;
@@ -250,6 +258,44 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b
         "mov.b64 db, {%2, %3};\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
+// e4m3 x e4m3 -> fp32 (tcgen05.mma kind::f8f6f4, K = 32 per instruction): A and B format
+// E4M3 (0) in bits 7-9 and 10-12, both operands K-major, D f32 in bits 4-5, N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
+// Four fp32 values to e4m3 (round to nearest, saturating to +-448) in one word, e0 in the
+// lowest byte (the lowest contraction index).  PTX cvt ... e4m3x2 puts its first source in
+// the upper byte of the pair.
+__device__ __forceinline__ uint32_t pack4_e4m3(float e0, float e1, float e2, float e3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(e1), "f"(e0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(e3), "f"(e2));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]

@@ -89,6 +89,27 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
                int H_kv, int N, int d, int dtype, float scale, int causal,
                const uint8_t *block_mask, void *stream);
 
+/*
+ * Forward on 8-bit float inputs.  The forward of fa_fwd_gqa with Q, K, V given as e4m3 codes
+ * (OCP 8-bit float E4M3: bias 7, 3 mantissa bits, largest 448, NaN = 0x7F/0xFF) and one scale
+ * per tensor: element x of Q stands for e4m3(x) * descale_q (likewise K, V).  QK^T and PV run
+ * as e4m3 tensor-core products (twice the bf16 rate); the softmax is fp32 as in fa_fwd; the
+ * probabilities are rounded to e4m3 before PV (their largest values scaled near the top of the
+ * e4m3 range), which bounds O's accuracy by e4m3's 3-bit mantissa rather than bf16's 8 bits.
+ *   q       : [B,H,N,d] e4m3 codes (device);  k, v : [B,H_kv,N,d] e4m3 codes (device).
+ *   o       : [B,H,N,d] bf16 output (device);  lse : [B,H,N] fp32 output, as in fa_fwd.
+ *   descale_q, descale_k, descale_v : finite, > 0.
+ *   workspace : at least fa_fwd_fp8_workspace_bytes() bytes, 16-byte aligned: V transposed
+ *               ([B,H_kv,d,N rounded up to 16]), written by this call.
+ *   block_mask : NULL for dense, otherwise as in fa_fwd_blocksparse.
+ * d is 64 or 128.  Other arguments and errors as fa_fwd_gqa.
+ */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d);
+int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+               int H_kv, int N, int d, float scale, float descale_q, float descale_k,
+               float descale_v, int causal, const uint8_t *block_mask, void *workspace,
+               size_t workspace_bytes, void *stream);
+
 /* Bytes of device scratch fa_bwd needs: D (fp32 [B,H,N]), rounded up to 256 bytes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 

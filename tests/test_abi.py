@@ -133,3 +133,21 @@ def test_decode_workspace_and_validation(lib):
     assert dec(d=80) == api.FA_ERR_UNSUPPORTED
     assert dec(kv_len=ctypes.c_void_p(18)) == api.FA_ERR_INVALID  # misaligned lengths
     assert dec(Nk=4096) == api.FA_ERR_INVALID  # several key ranges but no workspace
+
+
+def test_fp8_workspace_and_validation(lib):
+    p = ctypes.c_void_p(16)
+    # V transposed with keys rounded up to 16: [B, H_kv, d, 16 * ceil(N / 16)] bytes
+    assert api.fp8_workspace_bytes(1, 2, 100, 64) == (2 * 64 * 112 + 255) // 256 * 256
+    assert api.fp8_workspace_bytes(1, 32, 8192, 128) == 32 * 128 * 8192
+    assert lib.fa_fwd_fp8_workspace_bytes(1, 2, 100, 96) == 0
+
+    def f(ws=p, wsb=1 << 30, dq=0.1, H=4, Hkv=2, d=128):
+        return lib.fa_fwd_fp8(p, p, p, p, p, 1, H, Hkv, 256, d, 0.125, dq, 0.1, 0.1, 0, None,
+                              ws, wsb, None)
+    assert f(dq=0.0) == api.FA_ERR_INVALID
+    assert f(dq=float("inf")) == api.FA_ERR_INVALID
+    assert f(Hkv=3) == api.FA_ERR_INVALID
+    assert f(d=96) == api.FA_ERR_UNSUPPORTED
+    assert f(ws=None) == api.FA_ERR_INVALID
+    assert f(wsb=16) == api.FA_ERR_INVALID
