@@ -45,6 +45,7 @@ class Workload:
     sparse_p: Optional[float] = None  # Bernoulli keep-probability of off-diagonal mask blocks
     backward: bool = True
     h_kv: Optional[int] = None  # K/V heads (grouped-query attention); None means H
+    dropout: float = 0.0        # probability of dropping a probability (generator seed = seed)
 
     @property
     def kv_heads(self) -> int:
@@ -66,8 +67,9 @@ class Workload:
         kind = "block-sparse" if self.sparse_p is not None else ("causal" if self.causal else "dense")
         passes = "fwd+bwd" if self.backward else "fwd"
         heads = f"H={self.H}" if self.h_kv is None else f"H={self.H} H_kv={self.h_kv}"
+        drop = f", dropout {self.dropout}" if self.dropout else ""
         return (f"{self.name}: {passes} {kind} B={self.B} {heads} N={self.N} d={self.d} "
-                f"{self.dtype}")
+                f"{self.dtype}{drop}")
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -86,12 +88,15 @@ WORKLOADS: Dict[str, Workload] = {
     # the GPT-style 8k shape with grouped K/V heads: 32 query heads over 8 K/V heads
     "gqa_causal_d128_n8k": Workload("gqa_causal_d128_n8k", 1, 32, 8192, 128, "bf16", True, 6,
                                     qk_mult=2.0, h_kv=8),
+    # the GPT-style 8k training shape with dropout 0.1 on the attention probabilities
+    "dropout_causal_d128_n8k": Workload("dropout_causal_d128_n8k", 1, 32, 8192, 128, "bf16",
+                                        True, 9, qk_mult=2.0, dropout=0.1),
 }
 
 # the five workloads of the method's scope, in order; the rest extend it (grouped K/V heads)
 ORDER = ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k", "gpt_causal_d128_n8k",
          "blocksparse_d64_n16k"]
-EXTENSIONS = ["gqa_causal_d128_n8k"]
+EXTENSIONS = ["gqa_causal_d128_n8k", "dropout_causal_d128_n8k"]
 
 # e4m3 forward workloads: the GPT-style 8k shape with Q, K, V quantised per tensor
 FP8_WORKLOADS: Dict[str, Workload] = {

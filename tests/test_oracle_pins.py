@@ -501,3 +501,66 @@ def test_fp8_attention_is_attention_of_the_decoded_values():
     np.testing.assert_array_equal(a["lse"], b["lse"])
     for x in ("q", "k", "v"):  # the quantisation leaves every code finite
         assert not np.isnan(oracle.e4m3_to_f64(t[x])).any()
+
+
+# ---------------------------------------------------------------- dropout
+from oracle import dropout as odrop  # noqa: E402
+
+
+def test_philox_matches_numpy_generator():
+    # numpy's Philox is the same Philox4x64-10; its stream advances the counter before each
+    # block, so the block of counter c + 1 comes first
+    for ctr, key in (((5, 0, 0, 0), (12345, 678)), ((0, 7, 3, 0), (2 ** 63 + 5, 1)),
+                     ((123456789, 42, 9, 0), (0, 0))):
+        bg = np.random.Philox(counter=np.array(ctr, dtype=np.uint64),
+                              key=np.array(key, dtype=np.uint64))
+        raw = bg.random_raw(8)
+        c = np.array([[ctr[0] + 1, *ctr[1:]], [ctr[0] + 2, *ctr[1:]]], dtype=np.uint64)
+        mine = odrop.philox4x64_10(c, key).reshape(-1)
+        np.testing.assert_array_equal(mine, raw)
+
+
+def test_dropout_rate_and_threshold():
+    assert odrop.threshold(0.1) == 26 and odrop.threshold(0.0) == 0
+    with pytest.raises(ValueError):
+        odrop.threshold(1.0)
+    z = odrop.keep_mask(3, 512, 2048, seed=7, offset=1, t=64)  # p = 0.25
+    frac = 1.0 - z.mean()
+    sigma = math.sqrt(0.25 * 0.75 / z.size)
+    assert abs(frac - 0.25) < 5 * sigma
+    # different heads, rows, offsets give different decisions
+    assert not np.array_equal(z, odrop.keep_mask(4, 512, 2048, seed=7, offset=1, t=64))
+    assert not np.array_equal(z, odrop.keep_mask(3, 512, 2048, seed=7, offset=2, t=64))
+
+
+def test_dropout_zero_is_attention():
+    q, k, v, do = (rand((1, 2, 70, 8), s) for s in (120, 121, 122, 123))
+    a = odrop.attention_dropout(q, k, v, 0.4, 0.0, seed=1, causal=True, dout=do)
+    b = oracle.attention(q, k, v, 0.4, True, dout=do)
+    for name in ("o", "lse", "dq", "dk", "dv", "delta"):
+        np.testing.assert_allclose(a[name], b[name], atol=1e-12)
+
+
+def test_dropout_gradients_match_torch_autograd_and_delta_identity():
+    B, H, N, d, blk = 1, 2, 48, 8, 16
+    q, k, v, do = (rand((B, H, N, d), s) for s in (124, 125, 126, 127))
+    mask = make_block_mask(3, 13, 0.6).numpy()
+    p, seed, off = 0.3, 99, 5
+    res = odrop.attention_dropout(q, k, v, 0.35, p, seed, off, True, mask, blk, dout=do)
+    t = odrop.threshold(p)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    i = torch.arange(N)
+    keep = (i[None, :] <= i[:, None]) & torch.tensor(mask, dtype=torch.bool)[i // blk][:, i // blk]
+    outs = []
+    for h in range(H):
+        S = (0.35 * tq[0, h] @ tk[0, h].T).masked_fill(~keep, float("-inf"))
+        Z = torch.tensor(odrop.keep_mask(h, N, N, seed, off, t))
+        Pd = torch.softmax(S, -1) * Z * (256.0 / (256 - t))
+        outs.append(Pd @ tv[0, h])
+    O = torch.stack(outs)[None]
+    O.backward(torch.tensor(do))
+    np.testing.assert_allclose(res["o"], O.detach().numpy(), atol=1e-12)
+    for name, x in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(res[name], x.grad.numpy(), atol=1e-11)
+    # D = rowsum(P o dP) equals rowsum(dO o O) with dropout too
+    np.testing.assert_allclose(res["delta"], np.sum(do * res["o"], axis=-1), atol=1e-12)
