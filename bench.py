@@ -255,11 +255,11 @@ def run_gpu(args, w):
     lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream()
-    gqa = w.h_kv is not None
+    gqa = w.h_kv is not None or w.dropout > 0
     if gqa:
-        # grouped K/V heads: the forward kernel, then the whole grouped backward call (D, dK/dV
-        # summed over each group, dQ), timed as one unit
-        names = ["fa_fwd_kernel", "fa_bwd_gqa"]
+        # grouped K/V heads or dropout: the forward kernel, then the whole backward call (D,
+        # dK/dV, dQ), timed as one unit
+        names = ["fa_fwd_kernel", "fa_bwd_gqa" if w.dropout == 0 else "fa_bwd_dropout"]
         workspace = torch.empty(api.gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d),
                                 dtype=torch.uint8, device=dev)
         delta = workspace
@@ -269,13 +269,19 @@ def run_gpu(args, w):
         delta = torch.empty_like(lse)
 
     def fwd_call():
-        if gqa:
+        if w.dropout > 0:
+            api.fwd_dropout(q, k, v, w.dropout, w.seed, 0, w.scale, w.causal, mask, out=o,
+                            lse=lse)
+        elif gqa:
             api.fwd_gqa(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
         else:
             api.fwd(q, k, v, w.scale, w.causal, mask, out=o, lse=lse)
 
     def bwd_call():
-        if gqa:
+        if w.dropout > 0:
+            api.bwd_dropout(q, k, v, o, lse, do, w.dropout, w.seed, 0, w.scale, w.causal, mask,
+                            dq=dq, dk=dk, dv=dv, workspace=workspace)
+        elif gqa:
             api.bwd_gqa(q, k, v, o, lse, do, w.scale, w.causal, mask, dq=dq, dk=dk, dv=dv,
                         workspace=workspace)
         else:
@@ -325,7 +331,7 @@ def run_gpu(args, w):
     f = flops(w.B, w.H, w.N, w.d, w.causal, density)
     if gqa:
         f = {"fa_fwd_kernel": f["fa_fwd_kernel"],
-             "fa_bwd_gqa": sum(f.values()) - f["fa_fwd_kernel"]}
+             names[1]: sum(f.values()) - f["fa_fwd_kernel"]}
     step_flops = sum(f.values())
     value = world * step_flops * args.steps / (max_ms / 1e3) / 1e12
     per_kernel = {}

@@ -22,6 +22,7 @@ FA_NOALLOC_MAX_ROWS = 1 << 20  # B*H*N limit of fa_bwd_noalloc
 
 # exported names and their signatures, in the order include/fa.h declares them
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_u64 = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp]),
@@ -35,6 +36,10 @@ SIGNATURES = {
     "fa_bwd_gqa_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i,
                         _i, _i, _f, _i, _vp, _vp]),
+    "fa_fwd_dropout": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _f,
+                            _u64, _u64, _vp]),
+    "fa_bwd_dropout": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i,
+                            _i, _i, _f, _i, _vp, _f, _u64, _u64, _vp]),
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fa_bwd_dkdv": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
                          _vp, _vp]),
@@ -329,6 +334,50 @@ def decode(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_len=
                          B, H, Hkv, Nq, Nk, d, _dtype_code(q), float(scale), int(bool(causal)),
                          ws, nbytes, _stream(stream)), "fa_decode")
     return out, lse
+
+
+def fwd_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0,
+                scale: Optional[float] = None, causal: bool = False, block_mask=None, out=None,
+                lse=None, stream=None):
+    """O, LSE with dropout on the probabilities (fa_fwd_dropout); k, v may have H_kv heads."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    Hkv = _kv_check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_fwd_dropout(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
+                              _dev(lse, "lse"), B, H, Hkv, N, d, _dtype_code(q), float(scale),
+                              int(bool(causal)), mask_ptr, float(p_drop), int(seed), int(offset),
+                              _stream(stream)), "fa_fwd_dropout")
+    return out, lse
+
+
+def bwd_dropout(q, k, v, o, lse, dout, p_drop: float, seed: int, offset: int = 0,
+                scale: Optional[float] = None, causal: bool = False, block_mask=None, dq=None,
+                dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of the forward with dropout (fa_bwd_dropout), same dropout arguments."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    Hkv = _kv_check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = gqa_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
+    _check(lib.fa_bwd_dropout(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(o, "o", q),
+                              _dev(dout, "dout", q), _dev(lse, "lse"), _dev(dq, "dq", q),
+                              _dev(dk, "dk", k), _dev(dv, "dv", k), _dev(workspace, "workspace"),
+                              nbytes, B, H, Hkv, N, d, _dtype_code(q), float(scale),
+                              int(bool(causal)), mask_ptr, float(p_drop), int(seed), int(offset),
+                              _stream(stream)), "fa_bwd_dropout")
+    return dq, dk, dv
 
 
 def sync_status(stream=None) -> int:

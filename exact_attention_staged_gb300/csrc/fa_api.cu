@@ -124,6 +124,20 @@ int make_map_bytes(CUtensorMap *m, const void *base, long x, long y, long z, int
 
 int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 
+// Dropout decisions: drop probability p -> byte threshold t = nearest integer to 256 p (ties to
+// even), valid for 0 <= t <= 255; t = 0 turns dropout off.
+constexpr fa::DropSpec kNoDrop = {0u, 1.f, 0ull, 0ull};
+int make_drop(float p, unsigned long long seed, unsigned long long offset, fa::DropSpec *out) {
+    if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID;
+    const long t = std::lrint(static_cast<double>(p) * 256.0);
+    if (t < 0 || t > 255) return FA_ERR_INVALID;
+    out->t4 = static_cast<uint32_t>(t) * 0x01010101u;
+    out->keep_scale = static_cast<float>(256.0 / (256.0 - static_cast<double>(t)));
+    out->seed = seed;
+    out->offset = offset;
+    return FA_OK;
+}
+
 int check_heads(int H, int Hkv) {
     return (Hkv >= 1 && Hkv <= H && H % Hkv == 0) ? FA_OK : FA_ERR_INVALID;
 }
@@ -180,7 +194,7 @@ size_t part_bytes(const DkvSplit &sp, int B, int Hkv, int N, int d) {
 
 int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                int Hkv, int N, int d, int dtype, float scale, int causal, const uint8_t *mask,
-               void *stream) {
+               const fa::DropSpec &drop, void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
     if (rc != FA_OK) return rc;
     rc = check_heads(H, Hkv);
@@ -207,6 +221,7 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     p.head_group = head_group(BH, N, d, 2.0 / p.rep);  // K and V, shared by rep query heads
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
+    p.drop = drop;
     if (make_ctl(status, BH, p.T, &p.ctl) != FA_OK) return FA_ERR_INVALID;
     cudaError_t e = fa::launch_fwd(maps, p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -214,7 +229,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
 
 int bwd_params(const void *q, const void *k, const void *v, const void *dout, const float *lse,
                const float *delta, int B, int H, int Hkv, int N, int d, int dtype, float scale,
-               int causal, const uint8_t *mask, fa::Maps *maps, fa::BwdParams *p) {
+               int causal, const uint8_t *mask, const fa::DropSpec &drop, fa::Maps *maps,
+               fa::BwdParams *p) {
     int rc = check_shape(B, H, N, d, dtype, scale);
     if (rc != FA_OK) return rc;
     rc = check_heads(H, Hkv);
@@ -247,6 +263,7 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
     p->scale = scale;
     p->scale_log2 = scale * 1.4426950408889634f;
     p->causal = causal ? 1 : 0;
+    p->drop = drop;
     return make_ctl(status, BH, p->T, &p->ctl);
 }
 
@@ -255,11 +272,11 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
 int run_dkdv(const void *q, const void *k, const void *v, const void *dout, const float *lse,
              const float *delta, void *dk, void *dv, const DkvSplit &sp, float *part, int B,
              int H, int Hkv, int N, int d, int dtype, float scale, int causal,
-             const uint8_t *mask, void *stream) {
+             const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
     fa::Maps maps;
     fa::BwdParams p;
     int rc = bwd_params(q, k, v, dout, lse, delta, B, H, Hkv, N, d, dtype, scale, causal, mask,
-                        &maps, &p);
+                        drop, &maps, &p);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({dk, dv});
     if (rc != FA_OK) return rc;
@@ -281,11 +298,11 @@ int run_dkdv(const void *q, const void *k, const void *v, const void *dout, cons
 
 int run_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
            const float *delta, void *dq, int B, int H, int Hkv, int N, int d, int dtype,
-           float scale, int causal, const uint8_t *mask, void *stream) {
+           float scale, int causal, const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
     fa::Maps maps;
     fa::BwdParams p;
     int rc = bwd_params(q, k, v, dout, lse, delta, B, H, Hkv, N, d, dtype, scale, causal, mask,
-                        &maps, &p);
+                        drop, &maps, &p);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({dq});
     if (rc != FA_OK) return rc;
@@ -313,14 +330,38 @@ int run_preprocess(const void *o, const void *dout, float *delta, int B, int H, 
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
             const float *lse, void *dq, void *dk, void *dv, float *delta, const DkvSplit &sp,
             float *part, int B, int H, int Hkv, int N, int d, int dtype, float scale, int causal,
-            const uint8_t *mask, void *stream) {
+            const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
     int rc = run_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
     if (rc != FA_OK) return rc;
     rc = run_dkdv(q, k, v, dout, lse, delta, dk, dv, sp, part, B, H, Hkv, N, d, dtype, scale,
-                  causal, mask, stream);
+                  causal, mask, drop, stream);
     if (rc != FA_OK) return rc;
     return run_dq(q, k, v, dout, lse, delta, dq, B, H, Hkv, N, d, dtype, scale, causal, mask,
-                  stream);
+                  drop, stream);
+}
+
+// fa_bwd_gqa / fa_bwd_dropout: validation, workspace split, run_bwd.
+int bwd_entry(const void *q, const void *k, const void *v, const void *o, const void *dout,
+              const float *lse, void *dq, void *dk, void *dv, void *workspace,
+              size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
+              float scale, int causal, const uint8_t *block_mask, const fa::DropSpec &drop,
+              void *stream) {
+    int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_heads(H, H_kv);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace});
+    if (rc != FA_OK) return rc;
+    const size_t need_delta = delta_bytes(B, H, N);
+    const DkvSplit sp = dkdv_split(B, H, H_kv, N);  // once: the size check and the launch agree
+    const size_t need_part = part_bytes(sp, B, H_kv, N, d);
+    if (workspace_bytes < need_delta + need_part) return FA_ERR_INVALID;
+    float *delta = static_cast<float *>(workspace);
+    float *part = need_part ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                        need_delta)
+                            : nullptr;
+    return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, sp, part, B, H, H_kv, N, d, dtype,
+                   scale, causal, block_mask, drop, stream);
 }
 
 // Decode key ranges: as many per (K/V head, row group) as fit the whole grid into one wave of
@@ -374,20 +415,32 @@ extern "C" {
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
            int d, int dtype, float scale, int causal, void *stream) {
-    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, nullptr, stream);
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, nullptr, kNoDrop,
+                      stream);
 }
 
 int fa_fwd_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                        int H, int N, int d, int dtype, float scale, int causal,
                        const uint8_t *block_mask, void *stream) {
     if (block_mask == nullptr) return FA_ERR_INVALID;
-    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, block_mask, stream);
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, dtype, scale, causal, block_mask, kNoDrop,
+                      stream);
 }
 
 int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                int H_kv, int N, int d, int dtype, float scale, int causal,
                const uint8_t *block_mask, void *stream) {
     return fwd_common(q, k, v, o, lse, B, H, H_kv, N, d, dtype, scale, causal, block_mask,
+                      kNoDrop, stream);
+}
+
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                   int H, int H_kv, int N, int d, int dtype, float scale, int causal,
+                   const uint8_t *block_mask, float p_drop, unsigned long long seed,
+                   unsigned long long offset, void *stream) {
+    fa::DropSpec drop;
+    if (make_drop(p_drop, seed, offset, &drop) != FA_OK) return FA_ERR_INVALID;
+    return fwd_common(q, k, v, o, lse, B, H, H_kv, N, d, dtype, scale, causal, block_mask, drop,
                       stream);
 }
 
@@ -411,14 +464,14 @@ int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dout, c
                 const float *delta, void *dk, void *dv, int B, int H, int N, int d, int dtype,
                 float scale, int causal, const uint8_t *block_mask, void *stream) {
     return run_dkdv(q, k, v, dout, lse, delta, dk, dv, DkvSplit{1, 1}, nullptr, B, H, H, N, d,
-                    dtype, scale, causal, block_mask, stream);
+                    dtype, scale, causal, block_mask, kNoDrop, stream);
 }
 
 int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
               const float *delta, void *dq, int B, int H, int N, int d, int dtype, float scale,
               int causal, const uint8_t *block_mask, void *stream) {
     return run_dq(q, k, v, dout, lse, delta, dq, B, H, H, N, d, dtype, scale, causal, block_mask,
-                  stream);
+                  kNoDrop, stream);
 }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -433,22 +486,19 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
                const float *lse, void *dq, void *dk, void *dv, void *workspace,
                size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
                float scale, int causal, const uint8_t *block_mask, void *stream) {
-    int rc = check_shape(B, H, N, d, dtype, scale);
-    if (rc != FA_OK) return rc;
-    rc = check_heads(H, H_kv);
-    if (rc != FA_OK) return rc;
-    rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace});
-    if (rc != FA_OK) return rc;
-    const size_t need_delta = delta_bytes(B, H, N);
-    const DkvSplit sp = dkdv_split(B, H, H_kv, N);  // once: the size check and the launch agree
-    const size_t need_part = part_bytes(sp, B, H_kv, N, d);
-    if (workspace_bytes < need_delta + need_part) return FA_ERR_INVALID;
-    float *delta = static_cast<float *>(workspace);
-    float *part = need_part ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                                        need_delta)
-                            : nullptr;
-    return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, sp, part, B, H, H_kv, N, d, dtype,
-                   scale, causal, block_mask, stream);
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H_kv,
+                     N, d, dtype, scale, causal, block_mask, kNoDrop, stream);
+}
+
+int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
+                   float scale, int causal, const uint8_t *block_mask, float p_drop,
+                   unsigned long long seed, unsigned long long offset, void *stream) {
+    fa::DropSpec drop;
+    if (make_drop(p_drop, seed, offset, &drop) != FA_OK) return FA_ERR_INVALID;
+    return bwd_entry(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, H_kv,
+                     N, d, dtype, scale, causal, block_mask, drop, stream);
 }
 
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
@@ -466,7 +516,7 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
     rc = noalloc_scratch(dev, &delta);
     if (rc != FA_OK) return rc;
     return run_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, DkvSplit{1, 1}, nullptr, B, H, H, N,
-                   d, dtype, scale, causal, block_mask, stream);
+                   d, dtype, scale, causal, block_mask, kNoDrop, stream);
 }
 
 size_t fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d) {

@@ -180,7 +180,7 @@ struct DkvLayout {
     static constexpr int kComputeWarp0 = 2;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
@@ -416,6 +416,21 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         next_unit(p, kt, i0, hq_end, hq, i);
         for (; hq < hq_end; next_unit(p, kt, i0, hq_end, hq, i)) {
             const int e = n & 1;
+            uint32_t keep = 0;  // dropout: bit c set = query 32g + c of tile i keeps this key row
+            if constexpr (DROP) {
+                // lane l draws the bits of query 32g + l for the warp's 32 key rows (one
+                // generator block) before the scores are ready; the ballots hand lane r the bits
+                // of its own key row
+                const uint32_t mine = philox_keep_bits(
+                    static_cast<uint64_t>(kt) * 4 + quad,
+                    static_cast<uint64_t>(i * kTile + kGroupCols * g + lane),
+                    static_cast<uint64_t>(hq), p.drop);
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const uint32_t col = __ballot_sync(0xffffffffu, (mine >> r) & 1u);
+                    if (lane == r) keep = col;
+                }
+            }
             if (!mbar_wait_warp(&ld_full[e], (n >> 1) & 1, p.ctl, abort_flag) ||
                 !mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
@@ -450,7 +465,14 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     pk[2 * c + 1] = pack2<BF16>(pv[2], pv[3]);
                 }
             }
-            tmem_st16(tS, pk);
+            if constexpr (DROP) {  // dV sees the dropped probabilities, dS all of them
+                uint32_t pkd[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pkd[c] = keep_halves(pk[c], keep, c);
+                tmem_st16(tS, pkd);
+            } else {
+                tmem_st16(tS, pk);
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_ready);
@@ -463,6 +485,13 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(tdP, r);
                 tmem_wait_ld();
+                if constexpr (DROP) {  // dP of a dropped score is 0, of a kept one dP / (1 - p)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        r[c] = __float_as_uint(((keep >> c) & 1u)
+                                                   ? __uint_as_float(r[c]) * p.drop.keep_scale
+                                                   : 0.f);
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -500,7 +529,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                                                             p.splits + split) * p.kv_elems +
                                                   row_off;
             const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
-            const float mul = g < 2 ? 1.f : p.scale;
+            const float mul = g < 2 ? (DROP ? p.drop.keep_scale : 1.f) : p.scale;
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t a[32];
@@ -559,7 +588,7 @@ struct DqLayout {
     static constexpr int kComputeWarp0 = 3;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
@@ -789,6 +818,11 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             if (!tile_live(p, qt, j)) continue;
             const int b = n & 1;
             const uint32_t tS = tmem + lane_base + 128 * b + kGroupCols * g;
+            uint32_t keep = 0xffffffffu;  // dropout: bit e set = key 128 j + 32 g + e is kept
+            if constexpr (DROP)
+                keep = philox_keep_bits(static_cast<uint64_t>(j) * 4 + g,
+                                        static_cast<uint64_t>(q_row), static_cast<uint64_t>(bh),
+                                        p.drop);
             if (!mbar_wait_warp(&s_full[b], (n >> 1) & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
@@ -820,6 +854,13 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 uint32_t bv[32];
                 tmem_ld32(tdP, bv);
                 tmem_wait_ld();
+                if constexpr (DROP) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        bv[e] = __float_as_uint(((keep >> e) & 1u)
+                                                    ? __uint_as_float(bv[e]) * p.drop.keep_scale
+                                                    : 0.f);
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -914,7 +955,8 @@ cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long row
 template <int D, bool BF16>
 cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, cudaStream_t stream) {
     using L = DkvLayout<D>;
-    auto kern = fa_bwd_dkdv_kernel<D, BF16>;
+    auto kern = p.drop.t4 != 0 ? fa_bwd_dkdv_kernel<D, BF16, true>
+                               : fa_bwd_dkdv_kernel<D, BF16, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -926,7 +968,7 @@ cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, cudaStream_t stream
 template <int D, bool BF16>
 cudaError_t launch_dq_t(const Maps &m, const BwdParams &p, cudaStream_t stream) {
     using L = DqLayout<D>;
-    auto kern = fa_bwd_dq_kernel<D, BF16>;
+    auto kern = p.drop.t4 != 0 ? fa_bwd_dq_kernel<D, BF16, true> : fa_bwd_dq_kernel<D, BF16, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;

@@ -71,7 +71,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
@@ -300,6 +300,12 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int j = 0; j < jend; ++j) {
             if (!tile_live(p, qt, j)) continue;
+            uint32_t keep[4];  // dropout: keep bits of keys 32w .. 32w + 31 of this tile, drawn
+            if constexpr (DROP) {  // while the tensor core still works on S
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    keep[w] = philox_keep_bits(4u * j + w, q_row, bh, p.drop);
+            }
             if (!mbar_wait_warp(&s_full[t], cnt & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
@@ -345,9 +351,10 @@ __global__ void __launch_bounds__(320, 1)
                 for (int c = 0; c < 32; ++c) {
                     const float a = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c]), sl2, -mu));
                     const float b = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c + 1]), sl2, -mu));
-                    rs0 += a;
+                    rs0 += a;  // l sums every probability; only PV sees the dropped ones
                     rs1 += b;
                     pk[c] = pack2<BF16>(a, b);
+                    if constexpr (DROP) pk[c] = keep_halves(pk[c], keep[2 * h + (c >> 4)], c & 15);
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(320, 1)
             tc_fence_after();
         }
         if (ok) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? (DROP ? p.drop.keep_scale : 1.f) / l : 0.f;
             const bool valid = q_row < p.N;
             using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
             T *orow = reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.N + q_row) * D;
@@ -420,7 +427,7 @@ __global__ void __launch_bounds__(320, 1)
 template <int D, bool BF16>
 cudaError_t launch_fwd_t(const Maps &maps, const FwdParams &p, cudaStream_t stream) {
     using L = FwdLayout<D>;
-    auto kern = fa_fwd_kernel<D, BF16>;
+    auto kern = p.drop.t4 != 0 ? fa_fwd_kernel<D, BF16, true> : fa_fwd_kernel<D, BF16, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;

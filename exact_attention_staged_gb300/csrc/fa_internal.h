@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "philox.cuh"
 #include "sm100.cuh"
 
 namespace fa {
@@ -42,6 +43,7 @@ struct FwdParams {
     int rep;                  // query heads per K/V head: K/V head of query head bh is bh / rep
     float scale_log2;         // scale * log2(e)
     int causal;
+    DropSpec drop;            // dropout on the probabilities (drop.t4 == 0: none)
     Ctl ctl;
 };
 
@@ -65,6 +67,7 @@ struct BwdParams {
     float scale;              // softmax scale (dK and dQ carry it)
     float scale_log2;         // scale * log2(e)
     int causal;
+    DropSpec drop;            // the forward's dropout (drop.t4 == 0: none)
     Ctl ctl;
 };
 

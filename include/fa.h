@@ -152,6 +152,28 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
                float scale, int causal, const uint8_t *block_mask, void *stream);
 
 /*
+ * Dropout on the attention probabilities (FlashAttention paper detail: dropout is one of the
+ * operations fused into the kernel, O = dropout(softmax(S)) V; the pages give no generator).
+ * Score (q, k) of query head b*H + h is dropped with probability t / 256, t = the nearest
+ * integer to 256 * p_drop (ties to even), and a kept probability is scaled by 256 / (256 - t).
+ * The decision is byte (k mod 32) of Philox4x64-10 (Salmon et al., SC 2011) with counter
+ * (k div 32, q, b*H + h, 0) and key (seed, offset), kept when that byte is >= t; the backward
+ * regenerates the same decisions from the same arguments, so nothing is stored.
+ * fa_fwd_dropout: as fa_fwd_gqa; LSE is that of the scores (dropout does not change it).
+ * fa_bwd_dropout: as fa_bwd_gqa (same workspace) for the forward with these dropout arguments.
+ *   p_drop : 0 <= p_drop < 1 with t <= 255 (otherwise FA_ERR_INVALID); t = 0 is no dropout.
+ */
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                   int H, int H_kv, int N, int d, int dtype, float scale, int causal,
+                   const uint8_t *block_mask, float p_drop, unsigned long long seed,
+                   unsigned long long offset, void *stream);
+int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int dtype,
+                   float scale, int causal, const uint8_t *block_mask, float p_drop,
+                   unsigned long long seed, unsigned long long offset, void *stream);
+
+/*
  * The three stages of fa_bwd, exposed so a caller (or a profiler) can order or time them.
  * fa_bwd_preprocess: delta[b,h,i] = sum_k dout[b,h,i,k] * o[b,h,i,k] in fp32 (FlashAttention-2
  *   reading notes, Algorithm 2, precomputation; FlashAttention paper detail, "Technique 2").
