@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
+        {
             const uint32_t sSlot = smem_u32(smem + L::kSlotOff);
             const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
             const SDesc dK0 = sdesc_make(smem_u32(smem + L::kKOff), 16, 1024);
@@ -321,28 +322,28 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             const SDesc dSm = sdesc_make(sSlot, L::kBoxBytes, 1024);  // slot as MN-major B
             auto slot_of = [&](int l) { return l % L::kSlots; };
             auto full_wait = [&](int l) {
-                return mbar_wait(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
+                return mbar_wait_warp(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
             };
             auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d, A stationary
                 const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
+                    mma_ss_el(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_ts = [&](uint32_t d, uint32_t a_col, int l, bool acc) {  // K = 128 queries
                 const SDesc b = sdesc_add(dSm, slot_of(l) * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(d, a_col + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(b, kk * 2048),
+                    mma_ts_el(d, a_col + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(b, kk * 2048),
                            kIdescTS, (acc || kk > 0) ? 1u : 0u);
             };
             auto log_visit = [&](int hq, int i) {
-                if (p.ctl.visit_log != nullptr)
+                if (p.ctl.visit_log != nullptr && lane == 0)
                     p.ctl.visit_log[(static_cast<size_t>(hq) * p.T + i) * p.T + kt] |= 2;
             };
-            bool ok = mbar_wait(kv_full, 0, p.ctl, abort_flag);
+            bool ok = mbar_wait_warp(kv_full, 0, p.ctl, abort_flag);
             int hq = hq0, i = i0 - 1;
             next_unit(p, kt, i0, hq_end, hq, i);
             int n = 0;
@@ -350,9 +351,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 ok = full_wait(0) && full_wait(1);
                 if (ok) {
                     issue_ss(tS, dK0, 0);
-                    umma_commit(s_full);
+                    umma_commit_el(s_full);
                     issue_ss(tdP, dV0, 1);
-                    umma_commit(dp_full);
+                    umma_commit_el(dp_full);
                     log_visit(hq, i);
                 }
             }
@@ -361,43 +362,43 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 next_unit(p, kt, i0, hq_end, nhq, ni);
                 const bool more = nhq < hq_end;
                 const int lq = 2 * n, ldo = 2 * n + 1;  // this tile's Q and dO loads
-                if (!mbar_wait(p_ready, n & 1, p.ctl, abort_flag)) {
+                if (!mbar_wait_warp(p_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 issue_ts(tdV, tS, ldo, n > 0);  // dV += P^T dO
-                umma_commit(&empty[slot_of(ldo)]);
+                umma_commit_el(&empty[slot_of(ldo)]);
                 if (more) {
                     if (!full_wait(lq + 2)) {
                         ok = false;
                         break;
                     }
                     issue_ss(tS, dK0, lq + 2);  // S^T(n+1) = K Q^T
-                    umma_commit(s_full);
+                    umma_commit_el(s_full);
                     log_visit(nhq, ni);
                 }
-                if (!mbar_wait(ds_ready, n & 1, p.ctl, abort_flag)) {
+                if (!mbar_wait_warp(ds_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 issue_ts(tdK, tdP, lq, n > 0);  // dK += dS^T Q
-                umma_commit(&empty[slot_of(lq)]);
+                umma_commit_el(&empty[slot_of(lq)]);
                 if (more) {
                     if (!full_wait(ldo + 2)) {
                         ok = false;
                         break;
                     }
                     issue_ss(tdP, dV0, ldo + 2);  // dP^T(n+1) = V dO^T
-                    umma_commit(dp_full);
+                    umma_commit_el(dp_full);
                 }
                 hq = nhq;
                 i = ni;
                 ++n;
             }
-            if (ok && n > 0) umma_commit(fin);
-            umma_commit(drain);
+            if (ok && n > 0) umma_commit_el(fin);
+            umma_commit_el(drain);
             drain_wait(drain, 0, p.ctl);
         }
         __syncwarp();
@@ -681,7 +682,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         }
         __syncwarp();
     } else if (warp <= 2) {
-        if (lane == 0) {
+        // each issuing warp runs its loop in lockstep; one elected lane issues each MMA/commit
+        {
             const bool sq = warp == 1;  // warp 1: S and dQ; warp 2: dP
             const uint32_t sSlot = smem_u32(smem + L::kSlotOff);
             const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
@@ -691,14 +693,14 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             const SDesc dSm = sdesc_make(sSlot, L::kBoxBytes, 1024);  // slot as MN-major B
             auto slot_of = [&](int l) { return l % L::kSlots; };
             auto full_wait = [&](int l) {
-                return mbar_wait(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
+                return mbar_wait_warp(&full[slot_of(l)], (l / L::kSlots) & 1, p.ctl, abort_flag);
             };
             auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d
                 const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
+                    mma_ss_el(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
                 }
             };
             auto next_live = [&](int j) {
@@ -707,9 +709,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 return jend;
             };
             auto ds_wait = [&](int n) {
-                return mbar_wait(&ds_ready[n & 1], (n >> 1) & 1, p.ctl, abort_flag);
+                return mbar_wait_warp(&ds_ready[n & 1], (n >> 1) & 1, p.ctl, abort_flag);
             };
-            bool ok = mbar_wait(q_full, 0, p.ctl, abort_flag);
+            bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
             int j = next_live(-1);
             int j1 = j < jend ? next_live(j) : jend;  // tile n + 1
             int n = 0;
@@ -720,8 +722,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     if (ok) {
                         tc_fence_after();
                         issue_ss(tmem, dQa, 0);
-                        umma_commit(&s_full[0]);
-                        if (p.ctl.visit_log != nullptr)
+                        umma_commit_el(&s_full[0]);
+                        if (p.ctl.visit_log != nullptr && lane == 0)
                             p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
                     }
                     if (ok && j1 < jend) {
@@ -729,8 +731,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         if (ok) {
                             tc_fence_after();
                             issue_ss(tmem + 128, dQa, 2);
-                            umma_commit(&s_full[1]);
-                            if (p.ctl.visit_log != nullptr)
+                            umma_commit_el(&s_full[1]);
+                            if (p.ctl.visit_log != nullptr && lane == 0)
                                 p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j1] |= 4;
                         }
                     }
@@ -747,9 +749,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         const SDesc b = sdesc_add(dSm, slot_of(2 * n) * L::kTileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts(tdQ, buf + 32 * (kk >> 1) + 8 * (kk & 1),
+                            mma_ts_el(tdQ, buf + 32 * (kk >> 1) + 8 * (kk & 1),
                                    sdesc_add(b, kk * 2048), kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
-                        umma_commit(&empty[slot_of(2 * n)]);
+                        umma_commit_el(&empty[slot_of(2 * n)]);
                     }
                     if (j2 < jend) {  // S(n+2) into this buffer, after dQ(n) read it
                         if (!full_wait(2 * n + 4)) {
@@ -758,15 +760,15 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         }
                         tc_fence_after();
                         issue_ss(buf, dQa, 2 * n + 4);
-                        umma_commit(&s_full[n & 1]);
-                        if (p.ctl.visit_log != nullptr)
+                        umma_commit_el(&s_full[n & 1]);
+                        if (p.ctl.visit_log != nullptr && lane == 0)
                             p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j2] |= 4;
                     }
                     j = j1;
                     j1 = j2;
                     ++n;
                 }
-                if (ok && n > 0) umma_commit(fin);
+                if (ok && n > 0) umma_commit_el(fin);
             } else {
                 // dP(0); then per tile: once the groups are done with dP(n), dP(n+1)
                 if (ok && j < jend) {
@@ -774,8 +776,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     if (ok) {
                         tc_fence_after();
                         issue_ss(tdP, ddOa, 1);
-                        umma_commit(dp_full);
-                        umma_commit(&empty[slot_of(1)]);
+                        umma_commit_el(dp_full);
+                        umma_commit_el(&empty[slot_of(1)]);
                     }
                 }
                 while (ok && j < jend) {
@@ -790,15 +792,15 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         }
                         tc_fence_after();
                         issue_ss(tdP, ddOa, 2 * n + 3);
-                        umma_commit(dp_full);
-                        umma_commit(&empty[slot_of(2 * n + 3)]);
+                        umma_commit_el(dp_full);
+                        umma_commit_el(&empty[slot_of(2 * n + 3)]);
                     }
                     j = j1;
                     j1 = j1 < jend ? next_live(j1) : jend;
                     ++n;
                 }
             }
-            umma_commit(&drain[sq ? 0 : 1]);
+            umma_commit_el(&drain[sq ? 0 : 1]);
             drain_wait(&drain[sq ? 0 : 1], 0, p.ctl);
         }
         __syncwarp();

@@ -172,10 +172,11 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
+        {
             const uint32_t sQ = smem_u32(smem + L::kQOff);
             const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
-            bool ok = mbar_wait(q_full, 0, p.ctl, abort_flag);
+            bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
             tc_fence_after();
             int n = 0;
             int cnt[2] = {0, 0};
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss(tmem + t * 128, sdesc_add(a, off), sdesc_add(b, off), kIdescS,
+                    mma_ss_el(tmem + t * 128, sdesc_add(a, off), sdesc_add(b, off), kIdescS,
                            kk > 0 ? 1u : 0u);
                 }
             };
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 2048),
+                    mma_ts_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 2048),
                            kIdescPV, kk > 0 ? 1u : acc);
             };
 
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t kpar = (n / L::kSlots) & 1;
                 const int vs = (n + 1) % L::kSlots;
                 const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
-                if (!mbar_wait(&full[ks], kpar, p.ctl, abort_flag)) {
+                if (!mbar_wait_warp(&full[ks], kpar, p.ctl, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -223,13 +224,13 @@ __global__ void __launch_bounds__(320, 1)
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (prev_j >= 0 && prev_live[t]) {
                         if (!v_ready) {
-                            if (!mbar_wait(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                            if (!mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
                                 ok = false;
                                 break;
                             }
                             v_ready = true;
                         }
-                        if (!mbar_wait(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
+                        if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -239,15 +240,15 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     if (lv[t]) {
                         issue_s(t, ks);
-                        umma_commit(&s_full[t]);
-                        if (p.ctl.visit_log != nullptr)
+                        umma_commit_el(&s_full[t]);
+                        if (p.ctl.visit_log != nullptr && lane == 0)
                             p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
                                             j] |= 1;
                     }
                 }
                 if (!ok) break;
-                if (prev_j >= 0) umma_commit(&empty[prev_vs]);
-                umma_commit(&empty[ks]);
+                if (prev_j >= 0) umma_commit_el(&empty[prev_vs]);
+                umma_commit_el(&empty[ks]);
                 prev_j = j;
                 prev_live[0] = lv[0];
                 prev_live[1] = lv[1];
@@ -260,11 +261,11 @@ __global__ void __launch_bounds__(320, 1)
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (!prev_live[t]) continue;
                     if (!v_ready) {
-                        ok = mbar_wait(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
+                        ok = mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
                         v_ready = true;
                         if (!ok) break;
                     }
-                    if (!mbar_wait(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
+                    if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -272,14 +273,14 @@ __global__ void __launch_bounds__(320, 1)
                     issue_pv(t, prev_vs, cnt[t] > 0);
                     ++cnt[t];
                 }
-                if (ok) umma_commit(&empty[prev_vs]);
+                if (ok) umma_commit_el(&empty[prev_vs]);
             }
             if (ok) {
                 for (int t = 0; t < 2; ++t)
-                    if (cnt[t] > 0) umma_commit(&o_final[t]);
+                    if (cnt[t] > 0) umma_commit_el(&o_final[t]);
             }
             // every MMA issued above completes before the CTA releases TMEM and smem
-            umma_commit(drain);
+            umma_commit_el(drain);
             drain_wait(drain, 0, p.ctl);
         }
         __syncwarp();
