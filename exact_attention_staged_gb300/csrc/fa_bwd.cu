@@ -567,8 +567,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
 // Shared memory: Q_i and dO_i (stationary) and a ring of slots receiving K_0, V_0, K_1, V_1, ...
 // TMEM: two S buffers [0,128) and [128,256) (tile n uses buffer n % 2), dP [256,384),
 // dQ [384,384+d).  Group g packs its dS columns into the first 16 columns of its S quarter.
-// MMA order: warp 1 runs dQ(n), S(n+2), dQ(n+1), ...; warp 2 runs dP(n+1), dP(n+2), ... once
-// the groups are done with dP(n).  The next tile's S is already in TMEM while the groups work on
+// MMA order: warp 1 runs dQ(n), S(n+2), dQ(n+1), ...; warp 2 runs dP(n+1), dP(n+2), ... as soon
+// as every group has loaded dP(n) from TMEM (dp_read), so dP(n+1) overlaps the dS(n)
+// arithmetic.  The next tile's S is already in TMEM while the groups work on
 // tile n+1, and S(n+2) overwrites buffer n % 2 only after dQ(n) has read it.  Each S buffer has
 // its own dS-ready barrier, so neither issuer can fall two phases behind one.
 template <int D>
@@ -581,8 +582,8 @@ struct DqLayout {
     static constexpr int kdOOff = kTileBytes;
     static constexpr int kSlotOff = 2 * kTileBytes;
     static constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-    // q_full, full[S], empty[S], s_full[2], dp_full, ds_ready[2], final, drain[2]
-    static constexpr int kNumBars = 1 + 2 * kSlots + 8;
+    // q_full, full[S], empty[S], s_full[2], dp_full, ds_ready[2], final, drain[2], dp_read
+    static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kMiscOff + 16;  // the dynamic base is 1024-aligned (checked)
     static constexpr int kThreads = 96 + kComputeThreads;
@@ -611,6 +612,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     uint64_t *ds_ready = dp_full + 1;       // [2], one per S buffer
     uint64_t *fin = ds_ready + 2;
     uint64_t *drain = fin + 1;              // [2]
+    uint64_t *dp_read = drain + 2;          // every compute thread has loaded dP(n) from TMEM
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
 
@@ -632,6 +634,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         mbar_init(dp_full, 1);
         mbar_init(&ds_ready[0], kComputeThreads);
         mbar_init(&ds_ready[1], kComputeThreads);
+        mbar_init(dp_read, kComputeThreads);
         mbar_init(fin, 1);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
@@ -781,7 +784,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     }
                 }
                 while (ok && j < jend) {
-                    if (!ds_wait(n)) {
+                    // dP(n+1) may overwrite the dP buffer once every compute thread has loaded
+                    // dP(n) (dS goes to the S buffer), so it runs while dS(n) is computed
+                    if (!mbar_wait_warp(dp_read, n & 1, p.ctl, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -856,6 +861,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 uint32_t bv[32];
                 tmem_ld32(tdP, bv);
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(dp_read);  // the dP buffer is free for dP(n+1)
                 if constexpr (DROP) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
