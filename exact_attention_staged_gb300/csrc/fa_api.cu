@@ -666,7 +666,7 @@ int fa_debug_set_dkdv_splits(int splits) {
 }
 
 int fa_debug_set_fault(int mode) {
-    if (mode != 0 && mode != 1) return FA_ERR_INVALID;
+    if (mode < 0 || mode > 3) return FA_ERR_INVALID;
     std::lock_guard<std::mutex> lk(g_mu);
     g_fault_mode = mode;
     return FA_OK;

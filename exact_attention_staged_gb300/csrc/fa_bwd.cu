@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 int got = 0;
                 if (lane == 0) {
                     got = mbar_wait(&empty[s], ((l / L::kSlots) & 1) ^ 1, p.ctl, abort_flag);
-                    if (got) {
+                    // test hook: fault mode 2 leaves the first Q tile unloaded
+                    if (got && !(p.ctl.fault_mode == 2 && l == 0)) {
                         mbar_arrive_expect_tx(&full[s], L::kTileBytes);
                         uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
                         for (int b = 0; b < L::kBoxes; ++b)
@@ -305,8 +306,10 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             drain_wait(kv_full, 0, p.ctl);
             const int issued = 2 * n;
             const int first = issued > L::kSlots ? issued - L::kSlots : 0;
-            for (int l = first; l < issued; ++l)
+            for (int l = first; l < issued; ++l) {
+                if (p.ctl.fault_mode == 2 && l == 0) continue;  // never loaded
                 drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
+            }
         }
         cp_async_wait_all();
         __syncwarp();
@@ -669,6 +672,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (p.ctl.fault_mode == 3 && l == 0) continue;  // test hook: K_0 unloaded
                     mbar_arrive_expect_tx(&full[s], L::kTileBytes);
                     uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
                     for (int b = 0; b < L::kBoxes; ++b)
@@ -679,8 +683,10 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             if (!ok || *abort_flag) {
                 drain_wait(q_full, 0, p.ctl);
                 const int first = l > L::kSlots ? l - L::kSlots : 0;
-                for (int m = first; m < l; ++m)
+                for (int m = first; m < l; ++m) {
+                    if (p.ctl.fault_mode == 3 && m == 0) continue;  // never loaded
                     drain_wait(&full[m % L::kSlots], (m / L::kSlots) & 1, p.ctl);
+                }
             }
         }
         __syncwarp();

@@ -253,7 +253,9 @@ const char *fa_status_string(int code);
  *   that follow.  NULL turns logging off.
  * fa_debug_set_wait_limit_ns: bound on every device pipeline wait (default 2 s; 0 restores it).
  * fa_debug_set_fault: 0 = none; 1 = the forward's load warp skips the first key tile of each
- *   CTA, so the bounded waits run out and fa_sync_status() reports FA_ERR_TIMEOUT.
+ *   CTA; 2 = the dK/dV pass's load warp skips its first Q tile; 3 = the dQ pass's load warp
+ *   skips its first K tile.  The bounded waits then run out, the kernel returns early and
+ *   fa_sync_status() reports FA_ERR_TIMEOUT; other values: FA_ERR_INVALID.
  * fa_debug_set_dkdv_splits: 0 = automatic; s > 0 splits every K/V head's query group of
  *   fa_bwd_gqa over min(s, H / H_kv) dK/dV CTAs per key tile (changes the workspace size).
  *   Negative: FA_ERR_INVALID.

@@ -73,6 +73,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 128, 64, 1, 0.125, 0, None,
                       None) == api.FA_ERR_INVALID  # workspace too small
     assert lib.fa_debug_set_fault(5) == api.FA_ERR_INVALID
+    assert lib.fa_debug_set_fault(-1) == api.FA_ERR_INVALID
 
 
 def test_missing_library_fails_loudly(tmp_path):

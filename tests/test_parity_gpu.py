@@ -198,6 +198,34 @@ def test_timeout_is_reported_not_hung(cuda_lib):
     check_fwd(o, lse, ref, "after timeout")
 
 
+@pytest.mark.parametrize("mode,stage", [(2, "dkdv"), (3, "dq")])
+def test_backward_timeout_is_reported_not_hung(cuda_lib, mode, stage):
+    # the dK/dV (mode 2) or dQ (mode 3) load warp skips its first tile: the bounded waits run
+    # out after 50 ms, the kernel returns early, and the context stays usable
+    t = make_inputs(1, 1, 256, 64, torch.bfloat16, seed=52)
+    q, k, v, do = (t[x].to(DEV) for x in ("q", "k", "v", "do"))
+    o, lse = cuda_lib.fwd(q, k, v, 0.125)
+    delta = torch.empty_like(lse)
+    cuda_lib.bwd_preprocess(o, do, delta)
+    assert cuda_lib.sync_status() == 0
+    cuda_lib.debug_set_wait_limit_ns(50_000_000)
+    cuda_lib.debug_set_fault(mode)
+    try:
+        if stage == "dkdv":
+            cuda_lib.bwd_dkdv(q, k, v, do, lse, delta, torch.empty_like(q), torch.empty_like(q),
+                              0.125, False)
+        else:
+            cuda_lib.bwd_dq(q, k, v, do, lse, delta, torch.empty_like(q), 0.125, False)
+        assert cuda_lib.sync_status() == cuda_lib.FA_ERR_TIMEOUT
+    finally:
+        cuda_lib.debug_set_fault(0)
+        cuda_lib.debug_set_wait_limit_ns(0)
+    grads = cuda_lib.bwd(q, k, v, o, lse, do, 0.125)
+    assert cuda_lib.sync_status() == 0
+    ref = oracle.attention(t["q"], t["k"], t["v"], 0.125, dout=t["do"])
+    check_bwd(grads, ref, f"after {stage} timeout")
+
+
 def test_invalid_arguments_on_device(cuda_lib):
     q = torch.zeros(1, 1, 128, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(cuda_lib.FAError) as e:
