@@ -116,6 +116,7 @@ __device__ __forceinline__ void store_row16(void *dst, const uint32_t *v, float 
 constexpr int kGroups = 4;
 constexpr int kGroupCols = kTile / kGroups;  // 32
 constexpr int kComputeThreads = kGroups * 128;
+constexpr int kComputeWarps = kComputeThreads / 32;
 
 // ================================================================================ preprocess
 template <int D, bool BF16>
@@ -227,12 +228,12 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         }
         for (int e = 0; e < 2; ++e) {
             mbar_init(&ld_full[e], 32);   // one cp.async completion per lane of the load warp
-            mbar_init(&ld_empty[e], kComputeThreads);  // every compute thread, after its dS
+            mbar_init(&ld_empty[e], kComputeWarps);  // every compute warp, after its dS
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_ready, kComputeThreads);
-        mbar_init(ds_ready, kComputeThreads);
+        mbar_init(p_ready, kComputeWarps);
+        mbar_init(ds_ready, kComputeWarps);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -451,13 +452,18 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 uint32_t r[32];
                 tmem_ld32(tS, r);
                 tmem_wait_ld();
+                const float2 sc2 = make_float2(sl2, sl2);
+                const float2 nl2e = make_float2(-kLog2e, -kLog2e);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 lq = lv[c];
-                    float pv[4] = {ex2(fmaf(__uint_as_float(r[4 * c]), sl2, -lq.x * kLog2e)),
-                                   ex2(fmaf(__uint_as_float(r[4 * c + 1]), sl2, -lq.y * kLog2e)),
-                                   ex2(fmaf(__uint_as_float(r[4 * c + 2]), sl2, -lq.z * kLog2e)),
-                                   ex2(fmaf(__uint_as_float(r[4 * c + 3]), sl2, -lq.w * kLog2e))};
+                    const float2 x01 = ffma2(make_float2(__uint_as_float(r[4 * c]),
+                                                         __uint_as_float(r[4 * c + 1])),
+                                             sc2, fmul2(make_float2(lq.x, lq.y), nl2e));
+                    const float2 x23 = ffma2(make_float2(__uint_as_float(r[4 * c + 2]),
+                                                         __uint_as_float(r[4 * c + 3])),
+                                             sc2, fmul2(make_float2(lq.z, lq.w), nl2e));
+                    float pv[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
                     if (need_mask) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -477,9 +483,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             } else {
                 tmem_st16(tS, pk);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_ready);
+            mbar_arrive_warp_after_st(p_ready);
             if (!mbar_wait_warp(dp_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
@@ -500,19 +504,21 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 dq = dv[c];
-                    const float2 p0 = unpack2<BF16>(pk[2 * c]);
-                    const float2 p1 = unpack2<BF16>(pk[2 * c + 1]);
-                    w[2 * c] = pack2<BF16>(p0.x * (__uint_as_float(r[4 * c]) - dq.x),
-                                           p0.y * (__uint_as_float(r[4 * c + 1]) - dq.y));
-                    w[2 * c + 1] = pack2<BF16>(p1.x * (__uint_as_float(r[4 * c + 2]) - dq.z),
-                                               p1.y * (__uint_as_float(r[4 * c + 3]) - dq.w));
+                    const float2 s01 = fmul2(unpack2<BF16>(pk[2 * c]),
+                                             fsub2(make_float2(__uint_as_float(r[4 * c]),
+                                                               __uint_as_float(r[4 * c + 1])),
+                                                   make_float2(dq.x, dq.y)));
+                    const float2 s23 = fmul2(unpack2<BF16>(pk[2 * c + 1]),
+                                             fsub2(make_float2(__uint_as_float(r[4 * c + 2]),
+                                                               __uint_as_float(r[4 * c + 3])),
+                                                   make_float2(dq.z, dq.w)));
+                    w[2 * c] = pack2<BF16>(s01.x, s01.y);
+                    w[2 * c + 1] = pack2<BF16>(s23.x, s23.y);
                 }
                 tmem_st16(tdP, w);  // over columns already read
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(ds_ready);
-            mbar_arrive(&ld_empty[e]);
+            mbar_arrive_warp_after_st(ds_ready);
+            mbar_arrive_warp(&ld_empty[e]);
             ++n;
         }
         if (ok && n > 0) {
@@ -635,9 +641,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
         mbar_init(dp_full, 1);
-        mbar_init(&ds_ready[0], kComputeThreads);
-        mbar_init(&ds_ready[1], kComputeThreads);
-        mbar_init(dp_read, kComputeThreads);
+        mbar_init(&ds_ready[0], kComputeWarps);
+        mbar_init(&ds_ready[1], kComputeWarps);
+        mbar_init(dp_read, kComputeWarps);
         mbar_init(fin, 1);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
@@ -849,13 +855,19 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 tmem_ld32(tS, a);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float pv = ex2(fmaf(__uint_as_float(a[e]), sl2, -lrow));
-                    if (need_mask) {
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 x = ffma2(make_float2(__uint_as_float(a[e]),
+                                                       __uint_as_float(a[e + 1])),
+                                           make_float2(sl2, sl2), make_float2(-lrow, -lrow));
+                    pr[e] = ex2(x.x);
+                    pr[e + 1] = ex2(x.y);
+                }
+                if (need_mask) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
                         const int col = kv0 + e;
-                        if (col >= p.N || (p.causal && col > q_row)) pv = 0.f;
+                        if (col >= p.N || (p.causal && col > q_row)) pr[e] = 0.f;
                     }
-                    pr[e] = pv;
                 }
             }
             if (!mbar_wait_warp(dp_full, n & 1, p.ctl, abort_flag)) {
@@ -867,8 +879,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 uint32_t bv[32];
                 tmem_ld32(tdP, bv);
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(dp_read);  // the dP buffer is free for dP(n+1)
+                mbar_arrive_warp(dp_read);  // the dP buffer is free for dP(n+1)
                 if constexpr (DROP) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
@@ -877,15 +888,18 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                                                     : 0.f);
                 }
                 uint32_t w[16];
+                const float2 d2 = make_float2(drow, drow);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(bv[2 * e]) - drow),
-                                       pr[2 * e + 1] * (__uint_as_float(bv[2 * e + 1]) - drow));
+                for (int e = 0; e < 16; ++e) {
+                    const float2 ds = fmul2(make_float2(pr[2 * e], pr[2 * e + 1]),
+                                            fsub2(make_float2(__uint_as_float(bv[2 * e]),
+                                                              __uint_as_float(bv[2 * e + 1])),
+                                                  d2));
+                    w[e] = pack2<BF16>(ds.x, ds.y);
+                }
                 tmem_st16(tS, w);  // over columns already read
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&ds_ready[b]);
+            mbar_arrive_warp_after_st(&ds_ready[b]);
             ++n;
         }
         if (ok && n > 0) {

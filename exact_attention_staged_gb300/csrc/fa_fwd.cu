@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 128);
+            mbar_init(&p_full[t], 4);  // one arrival per softmax warp
             mbar_init(&o_final[t], 1);
         }
         mbar_init(drain, 1);
@@ -374,9 +374,7 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_st32(tO + cc * 32, o);
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[t]);
+            mbar_arrive_warp_after_st(&p_full[t]);
             ++cnt;
         }
         if (ok && cnt > 0) {
