@@ -11,17 +11,20 @@
 // FlashAttention post, "Block-Sparse FlashAttention").
 //
 // GB300 mapping (prior art on the pages is A100 mma.sync with warp split-Q; not used here):
-//   CTA = two query tiles of one head (256 rows), 320 threads, one CTA per SM:
+//   CTA = two query tiles of one head (256 rows), 384 threads, one CTA per SM:
 //     warp 0       TMA producer: Q tiles once, then K_j and V_j into a ring of smem slots
-//     warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS), O_t += P_t V_j (TS, P in TMEM)
-//     warps 2..5   softmax for query tile 0, one TMEM lane (= query row) per thread
-//     warps 6..9   softmax for query tile 1
+//     warp 1       MMA issuer (one elected lane): S_t = Q_t K_j^T (SS), O_t += P_t V_j (TS, P in
+//                  TMEM); warps 2, 3 idle, so that warps 0..3 form a warpgroup that hands
+//                  registers to the softmax warpgroups (setmaxnreg: 64 vs 216 per thread)
+//     warps 4..7   softmax for query tile 0, one TMEM lane (= query row) per thread
+//     warps 8..11  softmax for query tile 1
 //   TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 [256+d,256+2d).
 //   P_t is written as packed 16-bit pairs over the first 64 columns of S_t and read from
 //   there by the PV MMA, so P never touches shared memory.
 //   MMA issue order per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j): while one softmax
 //   group exponentiates, the tensor core works on the other group's products.
-//   The running max is kept in log2 units; O and l are rescaled only when the max grows by more
+//   The row max is a tree of three-input maxima; exponent arguments and row sums use paired
+//   fp32 instructions (f32x2).  The running max is kept in log2 units; O and l are rescaled only when the max grows by more
 //   than 8 (a factor 256).  This is exact: O~ and l always share the same reference max, and the
 //   final O~/l and L = m + log2(l) (converted to natural log) do not depend on which max it is.
 #include "fa_internal.h"
@@ -46,13 +49,29 @@ struct FwdLayout {
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 384;
     static constexpr uint32_t kTmemCols = 512;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     const uint32_t a = smem_u32(p);
     return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Largest of the 128 scores of a row: eight independent chains of three-input maxima.
+__device__ __forceinline__ float row_max128(const uint32_t *r) {
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(__uint_as_float(r[k]), __uint_as_float(r[8 + k]), __uint_as_float(r[16 + k]));
+#pragma unroll
+    for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            a[k] = fmax3(a[k], __uint_as_float(r[c + k]), __uint_as_float(r[c + 8 + k]));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], __uint_as_float(r[120 + k]));
+    return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
 }
 
 __device__ __forceinline__ bool tile_live(const FwdParams &p, int qt, int j) {
@@ -72,7 +91,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
 }
 
 template <int D, bool BF16, bool DROP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
     using L = FwdLayout<D>;
@@ -128,107 +147,145 @@ __global__ void __launch_bounds__(320, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // warpgroup 0 (load warp, MMA warp, two idle warps) gives registers to the two softmax
+    // warpgroups: 128 x 64 + 256 x 216 = 63488 of the 384 x 168 = 64512 the CTA is launched with
+    if (warp < 4) {
+        regs_dec<64>();
+        if (warp == 0) {
+            // ---------------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                uint8_t *sQ = smem + L::kQOff;
+                mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
+                for (int t = 0; t < (has1 ? 2 : 1); ++t)
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(sQ + t * L::kTileBytes + b * L::kBoxBytes, &tmq, b * 64,
+                                    (qt0 + t) * kTile, bh, q_full);
+                int n = 0;
+                bool ok = true;
+                for (int j = 0; j < jend && ok; ++j) {
+                    if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int s = n % L::kSlots;
+                        const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
+                        if (!mbar_wait(&empty[s], par, p.ctl, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!(p.ctl.fault_mode == 1 && n == 0)) {
+                            mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+                            uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
+                            for (int b = 0; b < L::kBoxes; ++b)
+                                tma_load_3d(dst + b * L::kBoxBytes, kv ? &tmv : &tmk, b * 64,
+                                            j * kTile, kvh, &full[s]);
+                        }
+                        ++n;
+                    }
+                }
+                if (!ok || *abort_flag) {
+                    // let every copy still in flight land before the CTA's shared memory goes away
+                    drain_wait(q_full, 0, p.ctl);
+                    const int first = n > L::kSlots ? n - L::kSlots : 0;
+                    for (int l = first; l < n; ++l) {
+                        if (p.ctl.fault_mode == 1 && l == 0) continue;
+                        drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
+                    }
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ---------------------------------------------------------------- MMA issuer
+            // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
+            {
+                const uint32_t sQ = smem_u32(smem + L::kQOff);
+                const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
+                bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
+                tc_fence_after();
+                int n = 0;
+                int cnt[2] = {0, 0};
+                int prev_j = -1;
+                bool prev_live[2] = {false, false};
+                int prev_vs = 0;
+                uint32_t prev_vpar = 0;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            uint8_t *sQ = smem + L::kQOff;
-            mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
-            for (int t = 0; t < (has1 ? 2 : 1); ++t)
-                for (int b = 0; b < L::kBoxes; ++b)
-                    tma_load_3d(sQ + t * L::kTileBytes + b * L::kBoxBytes, &tmq, b * 64,
-                                (qt0 + t) * kTile, bh, q_full);
-            int n = 0;
-            bool ok = true;
-            for (int j = 0; j < jend && ok; ++j) {
-                if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int s = n % L::kSlots;
-                    const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
-                    if (!mbar_wait(&empty[s], par, p.ctl, abort_flag)) {
+                // descriptors of the Q tiles and of slot 0; a slot or k-step only adds an offset
+                const SDesc dq0 = sdesc_make(sQ, 16, 1024);
+                const SDesc dk0 = sdesc_make(sSlots, 16, 1024);                // K: K-major
+                const SDesc dv0 = sdesc_make(sSlots, L::kBoxBytes, 1024);      // V: MN-major
+                auto issue_s = [&](int t, int ks) {
+                    const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
+                    const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
+                        mma_ss_el(tmem + t * 128, sdesc_add(a, off), sdesc_add(b, off), kIdescS,
+                               kk > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](int t, int vs, bool accumulate) {
+                    const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
+                    const uint32_t acc = accumulate ? 1u : 0u;
+    #pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 2048),
+                               kIdescPV, kk > 0 ? 1u : acc);
+                };
+
+                for (int j = 0; ok && j < jend; ++j) {
+                    const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
+                    if (!lv[0] && !lv[1]) continue;
+                    const int ks = n % L::kSlots;
+                    const uint32_t kpar = (n / L::kSlots) & 1;
+                    const int vs = (n + 1) % L::kSlots;
+                    const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
+                    if (!mbar_wait_warp(&full[ks], kpar, p.ctl, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (!(p.ctl.fault_mode == 1 && n == 0)) {
-                        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
-                        uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
-                        for (int b = 0; b < L::kBoxes; ++b)
-                            tma_load_3d(dst + b * L::kBoxBytes, kv ? &tmv : &tmk, b * 64,
-                                        j * kTile, kvh, &full[s]);
-                    }
-                    ++n;
-                }
-            }
-            if (!ok || *abort_flag) {
-                // let every copy still in flight land before the CTA's shared memory goes away
-                drain_wait(q_full, 0, p.ctl);
-                const int first = n > L::kSlots ? n - L::kSlots : 0;
-                for (int l = first; l < n; ++l) {
-                    if (p.ctl.fault_mode == 1 && l == 0) continue;
-                    drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
-        {
-            const uint32_t sQ = smem_u32(smem + L::kQOff);
-            const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
-            bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
-            tc_fence_after();
-            int n = 0;
-            int cnt[2] = {0, 0};
-            int prev_j = -1;
-            bool prev_live[2] = {false, false};
-            int prev_vs = 0;
-            uint32_t prev_vpar = 0;
-
-            // descriptors of the Q tiles and of slot 0; a slot or k-step only adds an offset
-            const SDesc dq0 = sdesc_make(sQ, 16, 1024);
-            const SDesc dk0 = sdesc_make(sSlots, 16, 1024);                // K: K-major
-            const SDesc dv0 = sdesc_make(sSlots, L::kBoxBytes, 1024);      // V: MN-major
-            auto issue_s = [&](int t, int ks) {
-                const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
-                const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss_el(tmem + t * 128, sdesc_add(a, off), sdesc_add(b, off), kIdescS,
-                           kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int vs, bool accumulate) {
-                const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
-                const uint32_t acc = accumulate ? 1u : 0u;
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 2048),
-                           kIdescPV, kk > 0 ? 1u : acc);
-            };
-
-            for (int j = 0; ok && j < jend; ++j) {
-                const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
-                if (!lv[0] && !lv[1]) continue;
-                const int ks = n % L::kSlots;
-                const uint32_t kpar = (n / L::kSlots) & 1;
-                const int vs = (n + 1) % L::kSlots;
-                const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
-                if (!mbar_wait_warp(&full[ks], kpar, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                bool v_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (prev_j >= 0 && prev_live[t]) {
-                        if (!v_ready) {
-                            if (!mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                    tc_fence_after();
+                    bool v_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (prev_j >= 0 && prev_live[t]) {
+                            if (!v_ready) {
+                                if (!mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                v_ready = true;
+                            }
+                            if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                                 ok = false;
                                 break;
                             }
+                            tc_fence_after();
+                            issue_pv(t, prev_vs, cnt[t] > 0);
+                            ++cnt[t];
+                        }
+                        if (lv[t]) {
+                            issue_s(t, ks);
+                            umma_commit_el(&s_full[t]);
+                            if (p.ctl.visit_log != nullptr && lane == 0)
+                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
+                                                j] |= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    if (prev_j >= 0) umma_commit_el(&empty[prev_vs]);
+                    umma_commit_el(&empty[ks]);
+                    prev_j = j;
+                    prev_live[0] = lv[0];
+                    prev_live[1] = lv[1];
+                    prev_vs = vs;
+                    prev_vpar = vpar;
+                    n += 2;
+                }
+                if (ok && prev_j >= 0) {
+                    bool v_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!prev_live[t]) continue;
+                        if (!v_ready) {
+                            ok = mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
                             v_ready = true;
+                            if (!ok) break;
                         }
                         if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                             ok = false;
@@ -238,55 +295,22 @@ __global__ void __launch_bounds__(320, 1)
                         issue_pv(t, prev_vs, cnt[t] > 0);
                         ++cnt[t];
                     }
-                    if (lv[t]) {
-                        issue_s(t, ks);
-                        umma_commit_el(&s_full[t]);
-                        if (p.ctl.visit_log != nullptr && lane == 0)
-                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
-                                            j] |= 1;
-                    }
+                    if (ok) umma_commit_el(&empty[prev_vs]);
                 }
-                if (!ok) break;
-                if (prev_j >= 0) umma_commit_el(&empty[prev_vs]);
-                umma_commit_el(&empty[ks]);
-                prev_j = j;
-                prev_live[0] = lv[0];
-                prev_live[1] = lv[1];
-                prev_vs = vs;
-                prev_vpar = vpar;
-                n += 2;
-            }
-            if (ok && prev_j >= 0) {
-                bool v_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!prev_live[t]) continue;
-                    if (!v_ready) {
-                        ok = mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
-                        v_ready = true;
-                        if (!ok) break;
-                    }
-                    if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(t, prev_vs, cnt[t] > 0);
-                    ++cnt[t];
+                if (ok) {
+                    for (int t = 0; t < 2; ++t)
+                        if (cnt[t] > 0) umma_commit_el(&o_final[t]);
                 }
-                if (ok) umma_commit_el(&empty[prev_vs]);
+                // every MMA issued above completes before the CTA releases TMEM and smem
+                umma_commit_el(drain);
+                drain_wait(drain, 0, p.ctl);
             }
-            if (ok) {
-                for (int t = 0; t < 2; ++t)
-                    if (cnt[t] > 0) umma_commit_el(&o_final[t]);
-            }
-            // every MMA issued above completes before the CTA releases TMEM and smem
-            umma_commit_el(drain);
-            drain_wait(drain, 0, p.ctl);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        regs_inc<216>();
         // ---------------------------------------------------------------- softmax groups
-        const int t = (warp - 2) >> 2;
+        const int t = (warp - 4) >> 2;
         const int quad = warp & 3;  // a warp may touch TMEM lanes [32*(warp%4), +32)
         const int row = quad * 32 + lane;
         const int qt = t == 0 ? qt0 : qt1;
@@ -320,19 +344,14 @@ __global__ void __launch_bounds__(320, 1)
             tmem_wait_ld();
             const int kv0 = j * kTile;
             const bool need_mask = (p.causal && j == qt) || (kv0 + kTile > p.N);
-            float mx = -INFINITY;
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int col = kv0 + c;
                     if (col >= p.N || (p.causal && col > q_row)) r[c] = __float_as_uint(-INFINITY);
-                    mx = fmaxf(mx, __uint_as_float(r[c]));
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c]));
             }
-            const float m_tile = mx * sl2;
+            const float m_tile = row_max128(r) * sl2;
             const float m_new = fmaxf(m, m_tile);
             const bool old_finite = m != -INFINITY;
             const bool grow = m_new > m + 8.0f;
@@ -344,21 +363,29 @@ __global__ void __launch_bounds__(320, 1)
             }
             const bool rescale = grow && old_finite;
             const float mu = m == -INFINITY ? 0.f : m;  // a row with nothing unmasked yet
-            float rs0 = 0.f, rs1 = 0.f;
+            // P~ = 2^(s * scale * log2(e) - mu) in pairs; l sums every probability (only PV sees
+            // the dropped ones); masked scores (-inf) give exactly 0
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            const float2 sc2 = make_float2(sl2, sl2), mu2 = make_float2(-mu, -mu);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float a = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c]), sl2, -mu));
-                    const float b = ex2(fmaf(__uint_as_float(r[64 * h + 2 * c + 1]), sl2, -mu));
-                    rs0 += a;  // l sums every probability; only PV sees the dropped ones
-                    rs1 += b;
-                    pk[c] = pack2<BF16>(a, b);
+                    const float2 x = ffma2(make_float2(__uint_as_float(r[64 * h + 2 * c]),
+                                                       __uint_as_float(r[64 * h + 2 * c + 1])),
+                                           sc2, mu2);
+                    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                    acc[c & 3] = fadd2(acc[c & 3], e);
+                    pk[c] = pack2<BF16>(e.x, e.y);
                     if constexpr (DROP) pk[c] = keep_halves(pk[c], keep[2 * h + (c >> 4)], c & 15);
                 }
                 tmem_st32(tS + 32 * h, pk);
             }
+            const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+            const float2 a = fadd2(a01, a23);
+            const float rs0 = a.x, rs1 = a.y;
             l += rs0 + rs1;
             if (__any_sync(0xffffffffu, rescale)) {
                 // The previous PV into O_t has completed (its commit preceded this S_t) and the

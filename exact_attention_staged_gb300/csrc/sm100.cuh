@@ -520,31 +520,6 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return d;
 }
 
-// 2^x for a pair of finite x <= 126 on the FMA pipe instead of the special-function unit, so a
-// softmax can split its exponentials between the two.  x is clamped below at -125 (the result
-// is then 2^-125 instead of a smaller value, which no 16-bit probability or fp32 row sum can
-// tell apart from zero next to the row's largest term, 2^0); n = round(x) is taken with the
-// 1.5 * 2^23 rounding constant, f = x - n lies in [-1/2, 1/2], 2^f comes from a degree-3
-// polynomial, and n is added to its exponent field.  The coefficients are the minimax fit of
-// the relative error on [-1/2, 1/2] computed by exact_attention_staged_gb300/fit_exp2.py
-// (linear programming on a dense grid); the relative error is below 7.5e-5, under half an ulp
-// of bf16 (2^-9) and of fp16 (2^-11).
-__device__ __forceinline__ float2 ex2_fma2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 kRound = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
-    const float2 t = fadd2(x, kRound);  // low mantissa bits of t hold round(x)
-    const float2 f = fsub2(x, fsub2(t, kRound));
-    float2 q = ffma2(f, make_float2(0x1.c3f888p-5f, 0x1.c3f888p-5f),
-                     make_float2(0x1.f0de1ep-3f, 0x1.f0de1ep-3f));
-    q = ffma2(q, f, make_float2(0x1.62f316p-1f, 0x1.62f316p-1f));
-    q = ffma2(q, f, make_float2(0x1.fff692p-1f, 0x1.fff692p-1f));
-    // adding round(x) << 23 to the bits of q scales it by 2^round(x); the constant's own bits
-    // shift out of the word
-    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
-                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // One mbarrier arrival per warp once every lane is past this point, its tensor-memory loads
 // waited for (the barrier is initialised with the number of arriving warps).
 __device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
