@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             // query q sees key k only when k <= q (causal) and q < N
             const int q_base = i * kTile + kGroupCols * g;
             const bool need_mask = (p.causal && i == kt) || (q_base + kGroupCols > p.N);
-            uint32_t pk[16];  // P^T of this row's 32 queries, packed 16-bit pairs
+            uint32_t pk[16];  // P^T of this row's 32 queries, packed 16-bit pairs (for dV)
+            float pf[32];     // the same in fp32 (for dS)
             {
                 uint32_t r[32];
                 tmem_ld32(tS, r);
@@ -473,6 +474,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     }
                     pk[2 * c] = pack2<BF16>(pv[0], pv[1]);
                     pk[2 * c + 1] = pack2<BF16>(pv[2], pv[3]);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) pf[4 * c + u] = pv[u];
                 }
             }
             if constexpr (DROP) {  // dV sees the dropped probabilities, dS all of them
@@ -504,11 +507,11 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 dq = dv[c];
-                    const float2 s01 = fmul2(unpack2<BF16>(pk[2 * c]),
+                    const float2 s01 = fmul2(make_float2(pf[4 * c], pf[4 * c + 1]),
                                              fsub2(make_float2(__uint_as_float(r[4 * c]),
                                                                __uint_as_float(r[4 * c + 1])),
                                                    make_float2(dq.x, dq.y)));
-                    const float2 s23 = fmul2(unpack2<BF16>(pk[2 * c + 1]),
+                    const float2 s23 = fmul2(make_float2(pf[4 * c + 2], pf[4 * c + 3]),
                                              fsub2(make_float2(__uint_as_float(r[4 * c + 2]),
                                                                __uint_as_float(r[4 * c + 3])),
                                                    make_float2(dq.z, dq.w)));
