@@ -207,8 +207,9 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     fa::Maps maps;
     const int BH = B * H;
     if (make_map(&maps.q, q, BH, N, d, dtype) || make_map(&maps.k, k, B * Hkv, N, d, dtype) ||
-        make_map(&maps.v, v, B * Hkv, N, d, dtype))
+        make_map(&maps.v, v, B * Hkv, N, d, dtype) || make_map(&maps.out0, o, BH, N, d, dtype))
         return FA_ERR_CUDA;
+    maps.out1 = maps.out0;
     fa::FwdParams p;
     p.o = o;
     p.lse = lse;
@@ -289,6 +290,14 @@ int run_dkdv(const void *q, const void *k, const void *v, const void *dout, cons
     p.units = B * Hkv * sp.splits;
     p.part = sp.splits > 1 ? part : nullptr;
     p.head_group = head_group(p.units, N, d, 2.0 * sp.chunk);  // Q and dO of chunk heads
+    if (sp.splits == 1) {  // dK, dV written by TMA; split groups write fp32 partials instead
+        if (make_map(&maps.out0, dk, B * Hkv, N, d, dtype) ||
+            make_map(&maps.out1, dv, B * Hkv, N, d, dtype))
+            return FA_ERR_CUDA;
+    } else {
+        maps.out0 = maps.k;
+        maps.out1 = maps.v;
+    }
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = fa::launch_bwd_dkdv(maps, p, d, dtype == FA_BF16, st);
     if (e == cudaSuccess && sp.splits > 1)
@@ -306,6 +315,8 @@ int run_dq(const void *q, const void *k, const void *v, const void *dout, const 
     if (rc != FA_OK) return rc;
     rc = check_ptrs({dq});
     if (rc != FA_OK) return rc;
+    if (make_map(&maps.out0, dq, B * H, N, d, dtype)) return FA_ERR_CUDA;
+    maps.out1 = maps.q;
     p.out0 = dq;
     cudaError_t e =
         fa::launch_bwd_dq(maps, p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));

@@ -32,11 +32,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    const uint32_t a = smem_u32(p);
-    return p + ((1024u - (a & 1023u)) & 1023u);
-}
-
 __device__ __forceinline__ bool tile_live(const BwdParams &p, int qt, int kt) {
     if (p.causal && kt > qt) return false;
     if (p.mask != nullptr && p.mask[qt * p.T + kt] == 0) return false;
@@ -75,20 +70,6 @@ __device__ __forceinline__ float lse_log2(const BwdParams &p, int bh, int row) {
 template <bool BF16>
 using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
-// Store 32 fp32 values (times `mul`) of one row as 16-bit values, 64 bytes.
-template <bool BF16>
-__device__ __forceinline__ void store_row32(void *dst, const uint32_t *v, float mul) {
-    uint32_t w[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    d[2] = make_uint4(w[8], w[9], w[10], w[11]);
-    d[3] = make_uint4(w[12], w[13], w[14], w[15]);
-}
-
 // Store 32 fp32 values (times `mul`) of one row as fp32, 128 bytes.
 __device__ __forceinline__ void store_row32_f32(float *dst, const uint32_t *v, float mul) {
     float4 *d = reinterpret_cast<float4 *>(dst);
@@ -96,18 +77,6 @@ __device__ __forceinline__ void store_row32_f32(float *dst, const uint32_t *v, f
     for (int e = 0; e < 8; ++e)
         d[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
                            __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
-}
-
-// Store 16 fp32 values (times `mul`) of one row as 16-bit values, 32 bytes.
-template <bool BF16>
-__device__ __forceinline__ void store_row16(void *dst, const uint32_t *v, float mul) {
-    uint32_t w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // Compute-group geometry shared by both backward kernels: four groups of four warps (one
@@ -186,7 +155,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv,
-                       const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmdo,
+                       const __grid_constant__ CUtensorMap tmdk,
+                       const __grid_constant__ CUtensorMap tmdv, const BwdParams p) {
     using L = DkvLayout<D>;
     constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);  // S^T, dP^T
     constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dV, dK
@@ -528,21 +499,46 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             ok = mbar_wait_warp(fin, 0, p.ctl, abort_flag);
             tc_fence_after();
         }
-        if (ok) {
-            // groups 0, 1 write the two column halves of dV; groups 2, 3 those of dK (x scale),
-            // as 16-bit values, or as fp32 partial sums when the K/V group is split
+        // groups 0, 1 hold the two column halves of dV; groups 2, 3 those of dK (x scale).
+        // With one split they are staged as 16-bit tiles in the (now idle) first two ring slots
+        // and written by TMA; a split K/V group writes fp32 partial sums directly.  Every compute
+        // warp reaches the named barrier, whether or not its waits succeeded.
+        const int half = g & 1;
+        const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
+        const float mul = g < 2 ? (DROP ? p.drop.keep_scale : 1.f) : p.scale;
+        if (p.part == nullptr) {
+            if (ok) {
+                uint8_t *stage = smem + L::kSlotOff + (g < 2 ? 0 : 1) * L::kTileBytes;
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    uint32_t a[32];
+                    if (n > 0) {
+                        tmem_ld32(tacc + 32 * cc, a);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e2 = 0; e2 < 32; ++e2) a[e2] = 0u;
+                    }
+                    const int col = half * (D / 2) + 32 * cc;
+                    st_box_row<BF16, 32>(stage + (col >> 6) * L::kBoxBytes, row, col & 63, a, mul);
+                }
+                fence_proxy_async_smem();
+            }
+            named_sync(1, kComputeThreads);
+            if (warp == L::kComputeWarp0 && lane == 0 && ok && *abort_flag == 0) {
+                const uint8_t *sdv = smem + L::kSlotOff, *sdk = sdv + L::kTileBytes;
+                for (int b2 = 0; b2 < L::kBoxes; ++b2) {
+                    tma_store_3d(&tmdv, sdv + b2 * L::kBoxBytes, b2 * 64, kt * kTile, kvh);
+                    tma_store_3d(&tmdk, sdk + b2 * L::kBoxBytes, b2 * 64, kt * kTile, kvh);
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        } else if (ok) {
             const bool valid = k_row < p.N;
-            using T = elem_t<BF16>;
-            const int half = g & 1;
-            const size_t row_off =
-                (static_cast<size_t>(kvh) * p.N + k_row) * D + half * (D / 2);
-            T *dst = reinterpret_cast<T *>(g < 2 ? p.out1 : p.out0) + row_off;
-            float *dstf = p.part == nullptr ? nullptr
-                                            : p.part + (static_cast<size_t>(g < 2 ? 1 : 0) *
-                                                            p.splits + split) * p.kv_elems +
-                                                  row_off;
-            const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
-            const float mul = g < 2 ? (DROP ? p.drop.keep_scale : 1.f) : p.scale;
+            const size_t row_off = (static_cast<size_t>(kvh) * p.N + k_row) * D + half * (D / 2);
+            float *dstf = p.part + (static_cast<size_t>(g < 2 ? 1 : 0) * p.splits + split) *
+                                       p.kv_elems + row_off;
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t a[32];
@@ -553,12 +549,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) a[e2] = 0u;
                 }
-                if (valid) {
-                    if (dstf != nullptr)
-                        store_row32_f32(dstf + 32 * cc, a, mul);
-                    else
-                        store_row32<BF16>(dst + 32 * cc, a, mul);
-                }
+                if (valid) store_row32_f32(dstf + 32 * cc, a, mul);
             }
         }
     }
@@ -606,7 +597,8 @@ template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv,
-                     const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmdo,
+                     const __grid_constant__ CUtensorMap tmdq, const BwdParams p) {
     using L = DqLayout<D>;
     constexpr uint32_t kIdescSS = idesc_f16(128, 128, BF16, false);  // S, dP
     constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dQ
@@ -909,12 +901,11 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             ok = mbar_wait_warp(fin, 0, p.ctl, abort_flag);
             tc_fence_after();
         }
+        // group g holds dQ columns [g*d/4, (g+1)*d/4) (times the softmax scale): staged as a
+        // 16-bit tile in the (now idle) first K/V ring slot and written by TMA.  Every compute
+        // warp reaches the named barrier, whether or not its waits succeeded.
         if (ok) {
-            // group g writes dQ columns [g*d/4, (g+1)*d/4) (times the softmax scale)
-            const bool valid = q_row < p.N;
-            using T = elem_t<BF16>;
-            T *dq = reinterpret_cast<T *>(p.out0) + (static_cast<size_t>(bh) * p.N + q_row) * D +
-                    g * (D / 4);
+            uint8_t *stage = smem + L::kSlotOff;
             const uint32_t tacc = tmem + lane_base + 384 + g * (D / 4);
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
@@ -926,8 +917,18 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) a[e] = 0u;
                 }
-                if (valid) store_row16<BF16>(dq + 16 * cc, a, p.scale);
+                const int col = g * (D / 4) + 16 * cc;
+                st_box_row<BF16, 16>(stage + (col >> 6) * L::kBoxBytes, row, col & 63, a, p.scale);
             }
+            fence_proxy_async_smem();
+        }
+        named_sync(1, kComputeThreads);
+        if (warp == L::kComputeWarp0 && lane == 0 && ok && *abort_flag == 0) {
+            for (int b2 = 0; b2 < L::kBoxes; ++b2)
+                tma_store_3d(&tmdq, smem + L::kSlotOff + b2 * L::kBoxBytes, b2 * 64, qt * kTile,
+                             bh);
+            bulk_commit();
+            bulk_wait_read_all();
         }
     }
 
@@ -993,7 +994,7 @@ cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, cudaStream_t stream
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(static_cast<long>(p.units) * p.T), L::kThreads, L::kAlloc,
-           stream>>>(m.q, m.k, m.v, m.dout, p);
+           stream>>>(m.q, m.k, m.v, m.dout, m.out0, m.out1, p);
     return cudaGetLastError();
 }
 
@@ -1005,7 +1006,7 @@ cudaError_t launch_dq_t(const Maps &m, const BwdParams &p, cudaStream_t stream) 
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(static_cast<long>(p.BH) * p.T), L::kThreads, L::kAlloc,
-           stream>>>(m.q, m.k, m.v, m.dout, p);
+           stream>>>(m.q, m.k, m.v, m.dout, m.out0, p);
     return cudaGetLastError();
 }
 

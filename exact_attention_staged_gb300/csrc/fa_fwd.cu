@@ -93,7 +93,8 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const
 template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmo, const FwdParams p) {
     using L = FwdLayout<D>;
     constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, true);
     constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false);
@@ -408,11 +409,14 @@ __global__ void __launch_bounds__(384, 1)
             ok = mbar_wait_warp(&o_final[t], 0, p.ctl, abort_flag);
             tc_fence_after();
         }
+        // A tile without live key tiles stages zeros: its Q tile must have landed first.
+        if (ok && cnt == 0) ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
+        // O_t = O~_t / l is staged as a 16-bit tile over Q_t (no MMA reads Q_t any more: every
+        // S_t was issued before the final PV_t) and written by TMA.  All four warps of the group
+        // reach the named barrier, whether or not their waits succeeded.
+        uint8_t *stage = smem + L::kQOff + t * L::kTileBytes;
         if (ok) {
             const float inv = l > 0.f ? (DROP ? p.drop.keep_scale : 1.f) / l : 0.f;
-            const bool valid = q_row < p.N;
-            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            T *orow = reinterpret_cast<T *>(p.o) + (static_cast<size_t>(bh) * p.N + q_row) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
@@ -423,22 +427,19 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv,
-                                       __uint_as_float(o[2 * e + 1]) * inv);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-                }
+                st_box_row<BF16, 32>(stage + (cc >> 1) * L::kBoxBytes, row, (cc & 1) * 32, o, inv);
             }
-            if (valid)
+            fence_proxy_async_smem();
+            if (q_row < p.N)
                 p.lse[static_cast<size_t>(bh) * p.N + q_row] =
                     l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+        named_sync(1 + t, 128);
+        if (quad == 0 && lane == 0 && ok && *abort_flag == 0 && qt * kTile < p.N) {
+            for (int b = 0; b < L::kBoxes; ++b)
+                tma_store_3d(&tmo, stage + b * L::kBoxBytes, b * 64, qt * kTile, bh);
+            bulk_commit();
+            bulk_wait_read_all();
         }
     }
 
@@ -459,7 +460,7 @@ cudaError_t launch_fwd_t(const Maps &maps, const FwdParams &p, cudaStream_t stre
     if (e != cudaSuccess) return e;
     const long grid = static_cast<long>(p.BH) * p.num_pairs;
     kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(maps.q, maps.k, maps.v,
-                                                                           p);
+                                                                           maps.out0, p);
     return cudaGetLastError();
 }
 

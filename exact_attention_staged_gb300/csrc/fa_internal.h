@@ -107,6 +107,7 @@ struct DecodeParams {
 
 struct Maps {
     CUtensorMap q, k, v, dout;
+    CUtensorMap out0, out1;   // outputs written by TMA: O (forward), dK and dV, or dQ
 };
 
 cudaError_t launch_fwd(const Maps &maps, const FwdParams &p, int d, bool bf16,

@@ -134,6 +134,24 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// TMA: 3-D tiled store of one box from shared memory (bulk-group completion).  The box is in
+// the map's swizzled layout; rows (y) or heads (z) past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int x,
+                                             int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -543,6 +561,25 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     } else {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// NV (16 or 32) consecutive values of one row (times mul) as 16-bit values into a 128-row x
+// 64-element box laid out as a TMA tile with the 128-byte swizzle (16-byte chunk c of row r at
+// r * 128 + (c ^ (r % 8)) * 16; the box is 1024-byte aligned).  col: the first element's column
+// within the box, a multiple of 8.
+template <bool BF16, int NV>
+__device__ __forceinline__ void st_box_row(uint8_t *box, int row, int col, const uint32_t *v,
+                                           float mul) {
+    uint32_t w[NV / 2];
+#pragma unroll
+    for (int e = 0; e < NV / 2; ++e)
+        w[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+#pragma unroll
+    for (int q = 0; q < NV / 8; ++q) {
+        const int chunk = ((col >> 3) + q) ^ (row & 7);
+        *reinterpret_cast<uint4 *>(box + row * 128 + chunk * 16) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
 }
 
