@@ -301,18 +301,14 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             };
             auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d, A stationary
                 const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss_el(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
-                }
+                if constexpr (D == 128)
+                    mma_ss_chain_k128(d, a, b, kIdescSS, 0u);
+                else
+                    mma_ss_chain_k64(d, a, b, kIdescSS, 0u);
             };
             auto issue_ts = [&](uint32_t d, uint32_t a_col, int l, bool acc) {  // K = 128 queries
-                const SDesc b = sdesc_add(dSm, slot_of(l) * L::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                    mma_ts_el(d, a_col + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_add(b, kk * 2048),
-                           kIdescTS, (acc || kk > 0) ? 1u : 0u);
+                mma_ts_chain_k128_g32(d, a_col, sdesc_add(dSm, slot_of(l) * L::kTileBytes),
+                                      kIdescTS, acc ? 1u : 0u);
             };
             auto log_visit = [&](int hq, int i) {
                 if (p.ctl.visit_log != nullptr && lane == 0)
@@ -707,11 +703,10 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             };
             auto issue_ss = [&](uint32_t d, SDesc a, int l) {  // 128 x 128 x d
                 const SDesc b = sdesc_add(dSk, slot_of(l) * L::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBoxBytes + (kk & 3) * 32;
-                    mma_ss_el(d, sdesc_add(a, off), sdesc_add(b, off), kIdescSS, kk > 0 ? 1u : 0u);
-                }
+                if constexpr (D == 128)
+                    mma_ss_chain_k128(d, a, b, kIdescSS, 0u);
+                else
+                    mma_ss_chain_k64(d, a, b, kIdescSS, 0u);
             };
             auto next_live = [&](int j) {
                 for (++j; j < jend; ++j)
@@ -756,11 +751,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     }
                     tc_fence_after();
                     {  // dQ += dS K_n, K = 128 keys
-                        const SDesc b = sdesc_add(dSm, slot_of(2 * n) * L::kTileBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ts_el(tdQ, buf + 32 * (kk >> 1) + 8 * (kk & 1),
-                                   sdesc_add(b, kk * 2048), kIdescTS, (n > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts_chain_k128_g32(tdQ, buf, sdesc_add(dSm, slot_of(2 * n) * L::kTileBytes),
+                                              kIdescTS, n > 0 ? 1u : 0u);
                         umma_commit_el(&empty[slot_of(2 * n)]);
                     }
                     if (j2 < jend) {  // S(n+2) into this buffer, after dQ(n) read it

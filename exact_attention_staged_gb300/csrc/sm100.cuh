@@ -366,6 +366,134 @@ __device__ __forceinline__ void mma_ts_el(uint32_t d_tmem, uint32_t a_tmem, SDes
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
 }
+// Whole GEMM chains in one instruction sequence with a single election: fewer issue slots per
+// MMA for the issuing warp, which shares its sub-partition with busy element-wise warps.
+// 128 x N x 128 from two K-major 128-byte-swizzled tiles of two 64-wide boxes each (16 KB
+// apart): D (+)= A B^T over 8 k-steps; only the first k-step uses `accumulate`.
+__device__ __forceinline__ void mma_ss_chain_k128(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 1024;\n\tadd.u32 bl, %3, 1024;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 1026;\n\tadd.u32 bl, %3, 1026;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 1028;\n\tadd.u32 bl, %3, 1028;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 1030;\n\tadd.u32 bl, %3, 1030;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc),
+        "r"(accumulate));
+}
+// The same over one 64-wide box (4 k-steps).
+__device__ __forceinline__ void mma_ss_chain_k64(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc),
+        "r"(accumulate));
+}
+// 128 x N x 128 with A (16-bit pairs) in tensor memory, 8 columns per k-step, and an
+// MN-major B whose k-steps are 2048 bytes apart: D (+)= A B over 8 k-steps.
+__device__ __forceinline__ void mma_ts_chain_k128(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 t, %4, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 16;\n\tadd.u32 bl, %2, 256;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 24;\n\tadd.u32 bl, %2, 384;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 32;\n\tadd.u32 bl, %2, 512;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 40;\n\tadd.u32 bl, %2, 640;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 48;\n\tadd.u32 bl, %2, 768;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 56;\n\tadd.u32 bl, %2, 896;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+// As mma_ts_chain_k128 with A packed by groups of 32 contraction indices, each group's
+// 16 columns 32 columns apart (k-step k at column 32 (k / 2) + 8 (k % 2)).
+__device__ __forceinline__ void mma_ts_chain_k128_g32(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 t, %4, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 db, {%2, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 128;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 32;\n\tadd.u32 bl, %2, 256;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 40;\n\tadd.u32 bl, %2, 384;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 64;\n\tadd.u32 bl, %2, 512;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 72;\n\tadd.u32 bl, %2, 640;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 96;\n\tadd.u32 bl, %2, 768;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 104;\n\tadd.u32 bl, %2, 896;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %4, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void umma_commit_el(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
