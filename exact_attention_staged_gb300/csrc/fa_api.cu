@@ -375,11 +375,13 @@ int bwd_entry(const void *q, const void *k, const void *v, const void *o, const 
                    scale, causal, block_mask, drop, stream);
 }
 
-// Decode key ranges: as many per (K/V head, row group) as fit the whole grid into one wave of
-// three 128-thread CTAs per SM on a 152-SM GB300 (a second, partial wave would leave most of the
-// GPU idle while it runs), but no range shorter than 256 keys; ranges are multiples of the
-// kernel's 32-key tile.
-constexpr long kDecodeWaveCtas = 3 * 152;
+// Decode key ranges: as many per (K/V head, row group) as give about twelve 128-thread CTAs per
+// SM of a 152-SM GB300, but no range shorter than 256 keys; ranges are multiples of the
+// kernel's 32-key tile.  A CTA works through its tiles with block-wide barriers, so more CTAs
+// per SM, not a deeper prefetch ring, keep the memory system busy (measured on the 8k-cache
+// workload: 3 CTAs per SM reach 0.49 of the copy bandwidth, 12 reach 0.57; a 5-stage ring was
+// slower).
+constexpr long kDecodeWaveCtas = 12 * 152;
 struct DecodeSplit {
     int splits, chunk, row_groups;
 };
