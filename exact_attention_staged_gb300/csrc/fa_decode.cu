@@ -283,20 +283,41 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     const int lane = threadIdx.x & 31;
     if (row >= total_rows) return;
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
+    // the ranges' statistics 32 at a time, lane s holding range s: M, the weights 2^(m_s - M)
+    // and l = sum w_s l_s by shuffles; then O = sum w_s O_s with every range's load issued
+    // before its use (the weights come from the lanes)
     float M = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, ml[static_cast<long>(s) * total_rows + row].x);
+    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+        const int s = s0 + lane;
+        const float m = s < p.splits ? ml[static_cast<long>(s) * total_rows + row].x : -INFINITY;
+        M = fmaxf(M, m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float lsum = 0.f, acc[kCols];
 #pragma unroll
     for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        const long prow = static_cast<long>(s) * total_rows + row;
-        const float2 st = ml[prow];
-        if (st.x == -INFINITY) continue;  // an empty range (also covers M = -inf)
-        const float w = ex2(st.x - M);
-        lsum = fmaf(w, st.y, lsum);
-        const float *src = p.part_o + prow * D + lane * kCols;
+    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+        const int s = s0 + lane;
+        float w = 0.f, lw = 0.f;
+        if (s < p.splits) {
+            const float2 st = ml[static_cast<long>(s) * total_rows + row];
+            if (st.x != -INFINITY) {  // an empty range (also covers M = -inf) weighs nothing
+                w = ex2(st.x - M);
+                lw = w * st.y;
+            }
+        }
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, src[c], acc[c]);
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        lsum += lw;
+        const int n = min(32, p.splits - s0);
+        for (int i = 0; i < n; ++i) {
+            const float wi = __shfl_sync(0xffffffffu, w, i);
+            const float *src = p.part_o + (static_cast<long>(s0 + i) * total_rows + row) * D +
+                               lane * kCols;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) acc[c] = fmaf(wi, src[c], acc[c]);
+        }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     T *dst = reinterpret_cast<T *>(p.o) + row * D + lane * kCols;

@@ -208,19 +208,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading and stride byte
-// offsets (all >> 4), fixed version bits 46..48 = 0b001, 128-byte swizzle in bits 61..63.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
 // Instruction descriptor for tcgen05.mma kind::f16 with an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
 //   15 A major (0 = K), 16 B major (0 = K, 1 = MN), 17-22 N >> 3, 24-28 M >> 4.
@@ -255,29 +242,6 @@ __device__ __forceinline__ SDesc sdesc_add(SDesc d, uint32_t byte_offset) {
     return d;
 }
 
-// D[tmem] (+)= A[smem] * B[smem], descriptors as halves (the issue path of the kernels)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b64 db, {%2, %3};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
-
 // e4m3 x e4m3 -> fp32 (tcgen05.mma kind::f8f6f4, K = 32 per instruction): A and B format
 // E4M3 (0) in bits 7-9 and 10-12, both operands K-major, D f32 in bits 4-5, N >> 3, M >> 4.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
@@ -285,28 +249,12 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b64 db, {%2, %3};\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
-
-// Elected-lane forms of the e4m3 MMAs (see mma_ss_el).
+// e4m3 MMAs issued by one lane chosen by elect.sync while the whole warp runs the issue loop in
+// lockstep (every lane computes the warp-uniform operands).  Keeping the issuing warp converged
+// lets its address arithmetic and waits run at full rate next to busy compute warps on the same
+// sub-partition, which a single-lane issue path inside a divergent branch does not (measured on
+// GB300: 74 vs 64 cycles per 128 x 128 x 16 MMA taking A from tensor memory, with three busy
+// warps alongside).
 __device__ __forceinline__ void mma_ss_f8_el(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
                                              uint32_t accumulate) {
     asm volatile(
@@ -339,33 +287,6 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float e0, float e1, float e2, flo
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// Elected-lane forms of mma_ss / mma_ts / umma_commit for an issue loop that the whole warp
-// runs in lockstep: every lane computes the (warp-uniform) operands, one lane chosen by
-// elect.sync issues.  Keeping the issuing warp converged lets its address arithmetic and waits
-// run at full rate next to busy compute warps on the same sub-partition, which a single-lane
-// issue path inside a divergent branch does not (measured on GB300: 74 vs 64 cycles per
-// 128 x 128 x 16 MMA taking A from tensor memory, with three busy warps alongside).
-__device__ __forceinline__ void mma_ss_el(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_ts_el(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b64 db, {%2, %3};\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
-}
 // Whole GEMM chains in one instruction sequence with a single election: fewer issue slots per
 // MMA for the issuing warp, which shares its sub-partition with busy element-wise warps.
 // 128 x N x 128 from two K-major 128-byte-swizzled tiles of two 64-wide boxes each (16 KB
@@ -502,37 +423,6 @@ __device__ __forceinline__ void umma_commit_el(uint64_t *bar) {
         : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive (once) on an mbarrier when every tcgen05 operation issued so far by this thread
-// has completed.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
 // Each thread of the warp reads its own lane (row) of tensor memory, 32 consecutive 32-bit
 // columns starting at taddr's column.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
@@ -559,12 +449,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
