@@ -58,22 +58,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-// Largest of the 128 scores of a row: eight independent chains of three-input maxima.
-__device__ __forceinline__ float row_max128(const uint32_t *r) {
-    float a[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        a[k] = fmax3(__uint_as_float(r[k]), __uint_as_float(r[8 + k]), __uint_as_float(r[16 + k]));
-#pragma unroll
-    for (int c = 24; c < 120; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            a[k] = fmax3(a[k], __uint_as_float(r[c + k]), __uint_as_float(r[c + 8 + k]));
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], __uint_as_float(r[120 + k]));
-    return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-}
-
 __device__ __forceinline__ bool tile_live(const FwdParams &p, int qt, int j) {
     if (qt >= p.T) return false;
     if (p.causal && j > qt) return false;

@@ -15,9 +15,10 @@
 //    leaving 17 binades below them before values flush to zero.  l sums the unrounded P~, so O
 //    and L = m - kOff + log2(l) are unchanged by the offset.
 //
-// CTA and TMEM layout as fa_fwd.cu: two query tiles (256 rows), 320 threads (TMA warp, MMA
-// warp, 2 x 4 softmax warps), S_t at columns [128 t, 128 t + 128), O_t at 256 + t d; P~_t packed
-// four per column over the first 32 columns of S_t.
+// CTA and TMEM layout as fa_fwd.cu: two query tiles (256 rows), 384 threads (TMA warp, MMA
+// warp, two idle warps whose registers go to the softmax warpgroups, 2 x 4 softmax warps), S_t
+// at columns [128 t, 128 t + 128), O_t at 256 + t d; P~_t packed four per column over the
+// first 32 columns of S_t.
 #include "fa_internal.h"
 
 #include <cmath>
@@ -40,7 +41,7 @@ struct Fp8Layout {
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 384;
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -71,7 +72,7 @@ __device__ __forceinline__ SDesc qk_desc(uint32_t saddr) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmvt, const Fp8FwdParams p) {
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
-            mbar_init(&p_full[t], 128);
+            mbar_init(&p_full[t], 4);  // one arrival per softmax warp
             mbar_init(&o_final[t], 1);
         }
         mbar_init(drain, 1);
@@ -129,96 +130,135 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            uint8_t *sQ = smem + L::kQOff;
-            mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
-            for (int t = 0; t < (has1 ? 2 : 1); ++t)
-                tma_load_3d(sQ + t * L::kTileBytes, &tmq, 0, (qt0 + t) * kTile, bh, q_full);
-            int n = 0;
-            bool ok = true;
-            for (int j = 0; j < jend && ok; ++j) {
-                if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
-                for (int kv = 0; kv < 2; ++kv) {  // K_j, then V^T_j
-                    const int s = n % L::kSlots;
-                    const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
-                    if (!mbar_wait(&empty[s], par, p.ctl, abort_flag)) {
+    // warpgroup 0 (load warp, MMA warp, two idle warps) gives registers to the two softmax
+    // warpgroups: 128 x 64 + 256 x 216 = 63488 of the 384 x 168 = 64512 the CTA is launched with
+    if (warp < 4) {
+        regs_dec<64>();
+        if (warp == 0) {
+            // ---------------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                uint8_t *sQ = smem + L::kQOff;
+                mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::kTileBytes);
+                for (int t = 0; t < (has1 ? 2 : 1); ++t)
+                    tma_load_3d(sQ + t * L::kTileBytes, &tmq, 0, (qt0 + t) * kTile, bh, q_full);
+                int n = 0;
+                bool ok = true;
+                for (int j = 0; j < jend && ok; ++j) {
+                    if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
+                    for (int kv = 0; kv < 2; ++kv) {  // K_j, then V^T_j
+                        const int s = n % L::kSlots;
+                        const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
+                        if (!mbar_wait(&empty[s], par, p.ctl, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[s], L::kTileBytes);
+                        uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
+                        if (kv == 0)
+                            tma_load_3d(dst, &tmk, 0, j * kTile, kvh, &full[s]);
+                        else
+                            tma_load_3d(dst, &tmvt, j * kTile, 0, kvh, &full[s]);
+                        ++n;
+                    }
+                }
+                if (!ok || *abort_flag) {
+                    drain_wait(q_full, 0, p.ctl);
+                    const int first = n > L::kSlots ? n - L::kSlots : 0;
+                    for (int l = first; l < n; ++l)
+                        drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            // ---------------------------------------------------------------- MMA issuer
+            // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
+            {
+                const uint32_t sQ = smem_u32(smem + L::kQOff);
+                const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
+                bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
+                tc_fence_after();
+                int n = 0;
+                int cnt[2] = {0, 0};
+                int prev_j = -1;
+                bool prev_live[2] = {false, false};
+                int prev_vs = 0;
+                uint32_t prev_vpar = 0;
+                const SDesc dq0 = qk_desc<D>(sQ);
+                const SDesc dk0 = qk_desc<D>(sSlots);
+                const SDesc dv0 = sdesc_make(sSlots, 16, 1024);  // V^T: 128-byte key rows
+                auto issue_s = [&](int t, int ks) {  // S_t = Q_t K^T: d / 32 steps of 32 bytes
+                    const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
+                    const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk)
+                        mma_ss_f8_el(tmem + t * 128, sdesc_add(a, kk * 32), sdesc_add(b, kk * 32),
+                                  kIdescS, kk > 0 ? 1u : 0u);
+                };
+                auto issue_pv = [&](int t, int vs, bool accumulate) {  // 4 steps of 32 keys
+                    const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
+                    const uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 32; ++kk)
+                        mma_ts_f8_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 32),
+                                  kIdescPV, kk > 0 ? 1u : acc);
+                };
+
+                for (int j = 0; ok && j < jend; ++j) {
+                    const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
+                    if (!lv[0] && !lv[1]) continue;
+                    const int ks = n % L::kSlots;
+                    const uint32_t kpar = (n / L::kSlots) & 1;
+                    const int vs = (n + 1) % L::kSlots;
+                    const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
+                    if (!mbar_wait_warp(&full[ks], kpar, p.ctl, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], L::kTileBytes);
-                    uint8_t *dst = smem + L::kSlotOff + s * L::kTileBytes;
-                    if (kv == 0)
-                        tma_load_3d(dst, &tmk, 0, j * kTile, kvh, &full[s]);
-                    else
-                        tma_load_3d(dst, &tmvt, j * kTile, 0, kvh, &full[s]);
-                    ++n;
-                }
-            }
-            if (!ok || *abort_flag) {
-                drain_wait(q_full, 0, p.ctl);
-                const int first = n > L::kSlots ? n - L::kSlots : 0;
-                for (int l = first; l < n; ++l)
-                    drain_wait(&full[l % L::kSlots], (l / L::kSlots) & 1, p.ctl);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
-        {
-            const uint32_t sQ = smem_u32(smem + L::kQOff);
-            const uint32_t sSlots = smem_u32(smem + L::kSlotOff);
-            bool ok = mbar_wait_warp(q_full, 0, p.ctl, abort_flag);
-            tc_fence_after();
-            int n = 0;
-            int cnt[2] = {0, 0};
-            int prev_j = -1;
-            bool prev_live[2] = {false, false};
-            int prev_vs = 0;
-            uint32_t prev_vpar = 0;
-            const SDesc dq0 = qk_desc<D>(sQ);
-            const SDesc dk0 = qk_desc<D>(sSlots);
-            const SDesc dv0 = sdesc_make(sSlots, 16, 1024);  // V^T: 128-byte key rows
-            auto issue_s = [&](int t, int ks) {  // S_t = Q_t K^T: d / 32 steps of 32 bytes
-                const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
-                const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk)
-                    mma_ss_f8_el(tmem + t * 128, sdesc_add(a, kk * 32), sdesc_add(b, kk * 32),
-                              kIdescS, kk > 0 ? 1u : 0u);
-            };
-            auto issue_pv = [&](int t, int vs, bool accumulate) {  // 4 steps of 32 keys
-                const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
-                const uint32_t acc = accumulate ? 1u : 0u;
-#pragma unroll
-                for (int kk = 0; kk < kTile / 32; ++kk)
-                    mma_ts_f8_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 32),
-                              kIdescPV, kk > 0 ? 1u : acc);
-            };
-
-            for (int j = 0; ok && j < jend; ++j) {
-                const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
-                if (!lv[0] && !lv[1]) continue;
-                const int ks = n % L::kSlots;
-                const uint32_t kpar = (n / L::kSlots) & 1;
-                const int vs = (n + 1) % L::kSlots;
-                const uint32_t vpar = ((n + 1) / L::kSlots) & 1;
-                if (!mbar_wait_warp(&full[ks], kpar, p.ctl, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                bool v_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (prev_j >= 0 && prev_live[t]) {
-                        if (!v_ready) {
-                            if (!mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                    tc_fence_after();
+                    bool v_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (prev_j >= 0 && prev_live[t]) {
+                            if (!v_ready) {
+                                if (!mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                v_ready = true;
+                            }
+                            if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                                 ok = false;
                                 break;
                             }
+                            tc_fence_after();
+                            issue_pv(t, prev_vs, cnt[t] > 0);
+                            ++cnt[t];
+                        }
+                        if (lv[t]) {
+                            issue_s(t, ks);
+                            umma_commit_el(&s_full[t]);
+                            if (p.ctl.visit_log != nullptr && lane == 0)
+                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
+                                                j] |= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    if (prev_j >= 0) umma_commit_el(&empty[prev_vs]);
+                    umma_commit_el(&empty[ks]);
+                    prev_j = j;
+                    prev_live[0] = lv[0];
+                    prev_live[1] = lv[1];
+                    prev_vs = vs;
+                    prev_vpar = vpar;
+                    n += 2;
+                }
+                if (ok && prev_j >= 0) {
+                    bool v_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!prev_live[t]) continue;
+                        if (!v_ready) {
+                            ok = mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
                             v_ready = true;
+                            if (!ok) break;
                         }
                         if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
                             ok = false;
@@ -228,54 +268,21 @@ __global__ void __launch_bounds__(320, 1)
                         issue_pv(t, prev_vs, cnt[t] > 0);
                         ++cnt[t];
                     }
-                    if (lv[t]) {
-                        issue_s(t, ks);
-                        umma_commit_el(&s_full[t]);
-                        if (p.ctl.visit_log != nullptr && lane == 0)
-                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
-                                            j] |= 1;
-                    }
+                    if (ok) umma_commit_el(&empty[prev_vs]);
                 }
-                if (!ok) break;
-                if (prev_j >= 0) umma_commit_el(&empty[prev_vs]);
-                umma_commit_el(&empty[ks]);
-                prev_j = j;
-                prev_live[0] = lv[0];
-                prev_live[1] = lv[1];
-                prev_vs = vs;
-                prev_vpar = vpar;
-                n += 2;
-            }
-            if (ok && prev_j >= 0) {
-                bool v_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!prev_live[t]) continue;
-                    if (!v_ready) {
-                        ok = mbar_wait_warp(&full[prev_vs], prev_vpar, p.ctl, abort_flag);
-                        v_ready = true;
-                        if (!ok) break;
-                    }
-                    if (!mbar_wait_warp(&p_full[t], cnt[t] & 1, p.ctl, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(t, prev_vs, cnt[t] > 0);
-                    ++cnt[t];
+                if (ok) {
+                    for (int t = 0; t < 2; ++t)
+                        if (cnt[t] > 0) umma_commit_el(&o_final[t]);
                 }
-                if (ok) umma_commit_el(&empty[prev_vs]);
+                umma_commit_el(drain);
+                drain_wait(drain, 0, p.ctl);
             }
-            if (ok) {
-                for (int t = 0; t < 2; ++t)
-                    if (cnt[t] > 0) umma_commit_el(&o_final[t]);
-            }
-            umma_commit_el(drain);
-            drain_wait(drain, 0, p.ctl);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        regs_inc<216>();
         // ---------------------------------------------------------------- softmax groups
-        const int t = (warp - 2) >> 2;
+        const int t = (warp - 4) >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int qt = t == 0 ? qt0 : qt1;
@@ -303,19 +310,14 @@ __global__ void __launch_bounds__(320, 1)
             tmem_wait_ld();
             const int kv0 = j * kTile;
             const bool need_mask = (p.causal && j == qt) || (kv0 + kTile > p.N);
-            float mx = -INFINITY;
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int col = kv0 + c;
                     if (col >= p.N || (p.causal && col > q_row)) r[c] = __float_as_uint(-INFINITY);
-                    mx = fmaxf(mx, __uint_as_float(r[c]));
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(r[c]));
             }
-            const float m_new = fmaxf(m, mx * sl2);
+            const float m_new = fmaxf(m, row_max128(r) * sl2);
             const bool old_finite = m != -INFINITY;
             const bool grow = m_new > m + kTau;
             float alpha = 1.f;
@@ -326,20 +328,24 @@ __global__ void __launch_bounds__(320, 1)
             }
             const bool rescale = grow && old_finite;
             const float bias = m == -INFINITY ? 0.f : kOff - m;  // nothing unmasked yet: P~ = 0
-            float rs0 = 0.f, rs1 = 0.f;
+            float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            const float2 sc2 = make_float2(sl2, sl2), b2 = make_float2(bias, bias);
             uint32_t pk[32];
 #pragma unroll
             for (int w = 0; w < 32; ++w) {
-                const float a = ex2(fmaf(__uint_as_float(r[4 * w]), sl2, bias));
-                const float b = ex2(fmaf(__uint_as_float(r[4 * w + 1]), sl2, bias));
-                const float c = ex2(fmaf(__uint_as_float(r[4 * w + 2]), sl2, bias));
-                const float d = ex2(fmaf(__uint_as_float(r[4 * w + 3]), sl2, bias));
-                rs0 += a + c;
-                rs1 += b + d;
-                pk[w] = pack4_e4m3(a, b, c, d);
+                const float2 x01 = ffma2(make_float2(__uint_as_float(r[4 * w]),
+                                                     __uint_as_float(r[4 * w + 1])), sc2, b2);
+                const float2 x23 = ffma2(make_float2(__uint_as_float(r[4 * w + 2]),
+                                                     __uint_as_float(r[4 * w + 3])), sc2, b2);
+                const float2 e01 = make_float2(ex2(x01.x), ex2(x01.y));
+                const float2 e23 = make_float2(ex2(x23.x), ex2(x23.y));
+                acc[0] = fadd2(acc[0], e01);
+                acc[1] = fadd2(acc[1], e23);
+                pk[w] = pack4_e4m3(e01.x, e01.y, e23.x, e23.y);
             }
             tmem_st32(tS, pk);
-            l += rs0 + rs1;
+            const float2 a = fadd2(acc[0], acc[1]);
+            l += a.x + a.y;
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
@@ -352,9 +358,7 @@ __global__ void __launch_bounds__(320, 1)
                     tmem_st32(tO + cc * 32, o);
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&p_full[t]);
+            mbar_arrive_warp_after_st(&p_full[t]);
             ++cnt;
         }
         if (ok && cnt > 0) {

@@ -511,6 +511,22 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// Largest of the 128 scores of a row: eight independent chains of three-input maxima.
+__device__ __forceinline__ float row_max128(const uint32_t *r) {
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        a[k] = fmax3(__uint_as_float(r[k]), __uint_as_float(r[8 + k]), __uint_as_float(r[16 + k]));
+#pragma unroll
+    for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            a[k] = fmax3(a[k], __uint_as_float(r[c + k]), __uint_as_float(r[c + 8 + k]));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = fmaxf(a[k], __uint_as_float(r[120 + k]));
+    return fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+}
+
 // Paired fp32 arithmetic (PTX f32x2 forms, sm_100 and later): one instruction for two lanes of
 // work, round to nearest.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
