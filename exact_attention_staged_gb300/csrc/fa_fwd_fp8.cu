@@ -189,18 +189,15 @@ __global__ void __launch_bounds__(384, 1)
                 auto issue_s = [&](int t, int ks) {  // S_t = Q_t K^T: d / 32 steps of 32 bytes
                     const SDesc a = sdesc_add(dq0, t * L::kTileBytes);
                     const SDesc b = sdesc_add(dk0, ks * L::kTileBytes);
-#pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk)
-                        mma_ss_f8_el(tmem + t * 128, sdesc_add(a, kk * 32), sdesc_add(b, kk * 32),
-                                  kIdescS, kk > 0 ? 1u : 0u);
+                    if constexpr (D == 128)
+                        mma_ss_f8_chain_k128(tmem + t * 128, a, b, kIdescS, 0u);
+                    else
+                        mma_ss_f8_chain_k64(tmem + t * 128, a, b, kIdescS, 0u);
                 };
                 auto issue_pv = [&](int t, int vs, bool accumulate) {  // 4 steps of 32 keys
-                    const SDesc b = sdesc_add(dv0, vs * L::kTileBytes);
-                    const uint32_t acc = accumulate ? 1u : 0u;
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 32; ++kk)
-                        mma_ts_f8_el(tmem + 256 + t * D, tmem + t * 128 + kk * 8, sdesc_add(b, kk * 32),
-                                  kIdescPV, kk > 0 ? 1u : acc);
+                    mma_ts_f8_chain_k128(tmem + 256 + t * D, tmem + t * 128,
+                                         sdesc_add(dv0, vs * L::kTileBytes), kIdescPV,
+                                         accumulate ? 1u : 0u);
                 };
 
                 for (int j = 0; ok && j < jend; ++j) {

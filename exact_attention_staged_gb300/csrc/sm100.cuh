@@ -249,32 +249,66 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// e4m3 MMAs issued by one lane chosen by elect.sync while the whole warp runs the issue loop in
-// lockstep (every lane computes the warp-uniform operands).  Keeping the issuing warp converged
-// lets its address arithmetic and waits run at full rate next to busy compute warps on the same
-// sub-partition, which a single-lane issue path inside a divergent branch does not (measured on
-// GB300: 74 vs 64 cycles per 128 x 128 x 16 MMA taking A from tensor memory, with three busy
-// warps alongside).
-__device__ __forceinline__ void mma_ss_f8_el(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
-                                             uint32_t accumulate) {
+// e4m3 GEMM chains with one election (as the f16 chains below): 128 x N x 128 from two
+// K-major 128-byte-swizzled tiles, 4 k-steps of 32 bytes.
+__device__ __forceinline__ void mma_ss_f8_chain_k128(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
-        "mov.b64 da, {%1, %2};\n\t"
-        "mov.b64 db, {%3, %4};\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+        "setp.ne.b32 t, %5, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+        "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc),
+        "r"(accumulate));
 }
-__device__ __forceinline__ void mma_ts_f8_el(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
-                                             uint32_t idesc, uint32_t accumulate) {
+// The same over 64 contraction bytes (2 k-steps).
+__device__ __forceinline__ void mma_ss_f8_chain_k64(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
+                                          uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\t"  // the instruction descriptor is never 0
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t"
+        "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+        "mov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc),
+        "r"(accumulate));
+}
+// 128 x N x 128 with A (four e4m3 per column) in tensor memory, 8 columns per k-step, and a
+// K-major B whose k-steps are 32 bytes apart.
+__device__ __forceinline__ void mma_ts_f8_chain_k128(uint32_t d_tmem, uint32_t a_tmem, SDesc b,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 t, %4, 0;\n\t"  // the instruction descriptor is never 0
         "mov.b64 db, {%2, %3};\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t"
+        "add.u32 at, %1, 8;\n\tadd.u32 bl, %2, 2;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 16;\n\tadd.u32 bl, %2, 4;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [at], db, %4, t;\n\t"
+        "add.u32 at, %1, 24;\n\tadd.u32 bl, %2, 6;\n\t"
+        "mov.b64 db, {bl, %3};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [at], db, %4, t;\n\t"
+        "}" ::"r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate));
 }
 
 // Four fp32 values to e4m3 (round to nearest, saturating to +-448) in one word, e0 in the
@@ -288,7 +322,12 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float e0, float e1, float e2, flo
 }
 
 // Whole GEMM chains in one instruction sequence with a single election: fewer issue slots per
-// MMA for the issuing warp, which shares its sub-partition with busy element-wise warps.
+// MMA for the issuing warp, which shares its sub-partition with busy element-wise warps.  The
+// whole warp runs the issue loop in lockstep (every lane computes the warp-uniform operands)
+// and one lane chosen by elect.sync issues: keeping the issuing warp converged lets its
+// address arithmetic and waits run at full rate next to busy compute warps, which a
+// single-lane issue path inside a divergent branch does not (measured on GB300: 74 vs 64
+// cycles per 128 x 128 x 16 MMA taking A from tensor memory, with three busy warps alongside).
 // 128 x N x 128 from two K-major 128-byte-swizzled tiles of two 64-wide boxes each (16 KB
 // apart): D (+)= A B^T over 8 k-steps; only the first k-step uses `accumulate`.
 __device__ __forceinline__ void mma_ss_chain_k128(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc,
