@@ -32,22 +32,25 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ bool tile_live(const BwdParams &p, int qt, int kt) {
+// bits: the CTA's mask column (dK/dV, bit = qt) or row (dQ, bit = kt) in shared memory, or
+// nullptr (read the bytes)
+__device__ __forceinline__ bool tile_live(const BwdParams &p, const uint32_t *bits, int qt, int kt,
+                                          int bit) {
     if (p.causal && kt > qt) return false;
-    if (p.mask != nullptr && p.mask[qt * p.T + kt] == 0) return false;
-    return true;
+    if (p.mask == nullptr) return true;
+    return bits != nullptr ? mask_bit(bits, bit) : p.mask[qt * p.T + kt] != 0;
 }
 
 // The dK/dV kernel walks the (query head, query tile) pairs of its key tile kt in order, query
 // tiles fastest: advance (hq, i) to the next live pair; hq reaches hq_end when none is left.
-__device__ __forceinline__ void next_unit(const BwdParams &p, int kt, int i0, int hq_end, int &hq,
-                                          int &i) {
+__device__ __forceinline__ void next_unit(const BwdParams &p, const uint32_t *bits, int kt, int i0,
+                                          int hq_end, int &hq, int &i) {
     for (;;) {
         if (++i >= p.T) {
             if (++hq >= hq_end) return;
             i = i0;
         }
-        if (tile_live(p, i, kt)) return;
+        if (tile_live(p, bits, i, kt, i)) return;
     }
 }
 
@@ -145,7 +148,8 @@ struct DkvLayout {
     // final, drain
     static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kAlloc = kMiscOff + 16;  // the dynamic base is 1024-aligned (checked)
+    static constexpr int kMaskOff = kMiscOff + 16;  // block-mask bits of the CTA's column / row
+    static constexpr int kAlloc = kMaskOff + kMaskSmemWords * 4;  // 1024-aligned base (checked)
     static constexpr int kThreads = 64 + kComputeThreads;
     static constexpr int kComputeWarp0 = 2;
 };
@@ -214,6 +218,11 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    uint32_t *mcol = nullptr;  // mask column kt as bits
+    if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
+        mcol = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+        mask_bits_load(mcol, p.mask + kt, p.T, p.T);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -233,8 +242,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         int n = 0;  // query tiles issued
         bool ok = true;
         int hq = hq0, i = i0 - 1;
-        next_unit(p, kt, i0, hq_end, hq, i);
-        for (; hq < hq_end && ok; next_unit(p, kt, i0, hq_end, hq, i)) {
+        next_unit(p, mcol, kt, i0, hq_end, hq, i);
+        for (; hq < hq_end && ok; next_unit(p, mcol, kt, i0, hq_end, hq, i)) {
             for (int x = 0; x < 2 && ok; ++x) {  // Q_i then dO_i
                 const int l = 2 * n + x;
                 const int s = l % L::kSlots;
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             };
             bool ok = mbar_wait_warp(kv_full, 0, p.ctl, abort_flag);
             int hq = hq0, i = i0 - 1;
-            next_unit(p, kt, i0, hq_end, hq, i);
+            next_unit(p, mcol, kt, i0, hq_end, hq, i);
             int n = 0;
             if (ok && hq < hq_end) {
                 ok = full_wait(0) && full_wait(1);
@@ -330,7 +339,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             }
             while (ok && hq < hq_end) {
                 int nhq = hq, ni = i;
-                next_unit(p, kt, i0, hq_end, nhq, ni);
+                next_unit(p, mcol, kt, i0, hq_end, nhq, ni);
                 const bool more = nhq < hq_end;
                 const int lq = 2 * n, ldo = 2 * n + 1;  // this tile's Q and dO loads
                 if (!mbar_wait_warp(p_ready, n & 1, p.ctl, abort_flag)) {
@@ -385,8 +394,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         int n = 0;
         bool ok = true;
         int hq = hq0, i = i0 - 1;
-        next_unit(p, kt, i0, hq_end, hq, i);
-        for (; hq < hq_end; next_unit(p, kt, i0, hq_end, hq, i)) {
+        next_unit(p, mcol, kt, i0, hq_end, hq, i);
+        for (; hq < hq_end; next_unit(p, mcol, kt, i0, hq_end, hq, i)) {
             const int e = n & 1;
             uint32_t keep = 0;  // dropout: bit c set = query 32g + c of tile i keeps this key row
             if constexpr (DROP) {
@@ -584,7 +593,8 @@ struct DqLayout {
     // q_full, full[S], empty[S], s_full[2], dp_full, ds_ready[2], final, drain[2], dp_read
     static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kAlloc = kMiscOff + 16;  // the dynamic base is 1024-aligned (checked)
+    static constexpr int kMaskOff = kMiscOff + 16;  // block-mask bits of the CTA's column / row
+    static constexpr int kAlloc = kMaskOff + kMaskSmemWords * 4;  // 1024-aligned base (checked)
     static constexpr int kThreads = 96 + kComputeThreads;
     static constexpr int kComputeWarp0 = 3;
 };
@@ -645,6 +655,11 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    uint32_t *mrow = nullptr;  // mask row qt as bits
+    if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
+        mrow = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+        mask_bits_load(mrow, p.mask + static_cast<long>(qt) * p.T, 1, p.T);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -662,7 +677,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             int l = 0;  // loads issued: K_n is load 2n, V_n load 2n + 1
             bool ok = true;
             for (int j = 0; j < jend && ok; ++j) {
-                if (!tile_live(p, qt, j)) continue;
+                if (!tile_live(p, mrow, qt, j, j)) continue;
                 for (int x = 0; x < 2; ++x, ++l) {
                     const int s = l % L::kSlots;
                     if (!mbar_wait(&empty[s], ((l / L::kSlots) & 1) ^ 1, p.ctl, abort_flag)) {
@@ -710,7 +725,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             };
             auto next_live = [&](int j) {
                 for (++j; j < jend; ++j)
-                    if (tile_live(p, qt, j)) return j;
+                    if (tile_live(p, mrow, qt, j, j)) return j;
                 return jend;
             };
             auto ds_wait = [&](int n) {
@@ -821,7 +836,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         int n = 0;
         bool ok = true;
         for (int j = 0; j < jend; ++j) {
-            if (!tile_live(p, qt, j)) continue;
+            if (!tile_live(p, mrow, qt, j, j)) continue;
             const int b = n & 1;
             const uint32_t tS = tmem + lane_base + 128 * b + kGroupCols * g;
             uint32_t keep = 0xffffffffu;  // dropout: bit e set = key 128 j + 32 g + e is kept

@@ -39,7 +39,8 @@ struct Fp8Layout {
     // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], drain
     static constexpr int kNumBars = 1 + 2 * kSlots + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kMaskOff = kMiscOff + 16;  // block-mask bits of the two query tiles
+    static constexpr int kBytes = kMaskOff + 2 * kMaskSmemWords * 4;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
     static constexpr int kThreads = 384;
 };
@@ -49,11 +50,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-__device__ __forceinline__ bool tile_live(const Fp8FwdParams &p, int qt, int j) {
+// rowbits: the query tile's mask row as bits in shared memory, or nullptr (read the bytes)
+__device__ __forceinline__ bool tile_live(const Fp8FwdParams &p, const uint32_t *rowbits, int qt,
+                                          int j) {
     if (qt >= p.T) return false;
     if (p.causal && j > qt) return false;
-    if (p.mask != nullptr && p.mask[qt * p.T + j] == 0) return false;
-    return true;
+    if (p.mask == nullptr) return true;
+    return rowbits != nullptr ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
@@ -125,6 +128,14 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    uint32_t *mbits = nullptr;  // mask rows of qt0 and qt1, kMaskSmemWords words each
+    if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
+        mbits = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+        mask_bits_load(mbits, p.mask + static_cast<long>(qt0) * p.T, 1, p.T);
+        if (has1)
+            mask_bits_load(mbits + kMaskSmemWords, p.mask + static_cast<long>(qt1) * p.T, 1, p.T);
+    }
+    const uint32_t *mrow0 = mbits, *mrow1 = mbits != nullptr ? mbits + kMaskSmemWords : nullptr;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -144,7 +155,7 @@ __global__ void __launch_bounds__(384, 1)
                 int n = 0;
                 bool ok = true;
                 for (int j = 0; j < jend && ok; ++j) {
-                    if (!tile_live(p, qt0, j) && !tile_live(p, qt1, j)) continue;
+                    if (!tile_live(p, mrow0, qt0, j) && !tile_live(p, mrow1, qt1, j)) continue;
                     for (int kv = 0; kv < 2; ++kv) {  // K_j, then V^T_j
                         const int s = n % L::kSlots;
                         const uint32_t par = ((n / L::kSlots) & 1) ^ 1;
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__(384, 1)
                 };
 
                 for (int j = 0; ok && j < jend; ++j) {
-                    const bool lv[2] = {tile_live(p, qt0, j), tile_live(p, qt1, j)};
+                    const bool lv[2] = {tile_live(p, mrow0, qt0, j), tile_live(p, mrow1, qt1, j)};
                     if (!lv[0] && !lv[1]) continue;
                     const int ks = n % L::kSlots;
                     const uint32_t kpar = (n / L::kSlots) & 1;
@@ -283,6 +294,7 @@ __global__ void __launch_bounds__(384, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int qt = t == 0 ? qt0 : qt1;
+        const uint32_t *mrow = t == 0 ? mrow0 : mrow1;
         const int q_row = qt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem + lane_base + t * 128;
@@ -293,7 +305,7 @@ __global__ void __launch_bounds__(384, 1)
         int cnt = 0;
         bool ok = true;
         for (int j = 0; j < jend; ++j) {
-            if (!tile_live(p, qt, j)) continue;
+            if (!tile_live(p, mrow, qt, j)) continue;
             if (!mbar_wait_warp(&s_full[t], cnt & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;

@@ -13,6 +13,32 @@ namespace fa {
 
 constexpr int kTile = 128;  // query rows / key rows per tile, also the block-mask granularity
 
+// Block-mask bits in shared memory.  A CTA walks one row (forward, dQ: its query tiles' key
+// tiles) or one column (dK/dV: its key tile's query tiles) of the [T][T] byte mask, and every
+// warp role re-scans it; read from global memory that is one dependent load per tile visited,
+// and a column's bytes are T bytes apart, so each one is a round trip to L2.  The CTA copies its
+// row or column once, 32 tiles per ballot, as bits; masks wider than kMaskSmemTiles tiles
+// (N > 524288) are read from global memory as before.
+constexpr int kMaskSmemTiles = 4096;
+constexpr int kMaskSmemWords = kMaskSmemTiles / 32;
+
+// Every warp of the CTA calls this (warp-uniform): bit i of bits[] = (src[i * stride] != 0) for
+// i < T; warp w writes words w, w + warps, ...
+__device__ __forceinline__ void mask_bits_load(uint32_t *bits, const uint8_t *src, long stride,
+                                               int T) {
+    const int warps = static_cast<int>(blockDim.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    for (int w = static_cast<int>(threadIdx.x >> 5); w < (T + 31) / 32; w += warps) {
+        const int i = 32 * w + lane;
+        const bool live = i < T && src[static_cast<long>(i) * stride] != 0;
+        const uint32_t word = __ballot_sync(0xffffffffu, live);
+        if (lane == 0) bits[w] = word;
+    }
+}
+__device__ __forceinline__ bool mask_bit(const uint32_t *bits, int i) {
+    return ((bits[i >> 5] >> (i & 31)) & 1u) != 0;
+}
+
 // CTA order: heads are taken in groups of `group` so that the tiles streamed by the CTAs that
 // run at the same time (K/V of the forward, Q/dO of dK/dV, K/V of dQ) stay within a slice of
 // L2; inside a group the work unit (query-tile pair or tile) advances slowest, longest first.
