@@ -32,13 +32,14 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// bits: the CTA's mask column (dK/dV, bit = qt) or row (dQ, bit = kt) in shared memory, or
-// nullptr (read the bytes)
+// bits: where the CTA keeps its mask column (dK/dV, bit = qt) or row (dQ, bit = kt) in shared
+// memory when the mask is at most kMaskSmemTiles wide (a constant address: nothing stays live in
+// a register between calls); wider masks are read from global memory
 __device__ __forceinline__ bool tile_live(const BwdParams &p, const uint32_t *bits, int qt, int kt,
                                           int bit) {
     if (p.causal && kt > qt) return false;
     if (p.mask == nullptr) return true;
-    return bits != nullptr ? mask_bit(bits, bit) : p.mask[qt * p.T + kt] != 0;
+    return p.T <= kMaskSmemTiles ? mask_bit(bits, bit) : p.mask[qt * p.T + kt] != 0;
 }
 
 // The dK/dV kernel walks the (query head, query tile) pairs of its key tile kt in order, query
@@ -218,11 +219,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    uint32_t *mcol = nullptr;  // mask column kt as bits
-    if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
-        mcol = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
-        mask_bits_load(mcol, p.mask + kt, p.T, p.T);
-    }
+    uint32_t *const mcol = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);  // column kt
+    if (p.mask != nullptr && p.T <= kMaskSmemTiles) mask_bits_load(mcol, p.mask + kt, p.T, p.T);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -655,11 +653,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    uint32_t *mrow = nullptr;  // mask row qt as bits
-    if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
-        mrow = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+    uint32_t *const mrow = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);  // row qt
+    if (p.mask != nullptr && p.T <= kMaskSmemTiles)
         mask_bits_load(mrow, p.mask + static_cast<long>(qt) * p.T, 1, p.T);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -59,13 +59,14 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-// rowbits: the query tile's mask row as bits in shared memory, or nullptr (read the bytes)
+// rowbits: where the query tile's mask row is kept as bits in shared memory when the mask is
+// at most kMaskSmemTiles wide; wider masks are read from global memory
 __device__ __forceinline__ bool tile_live(const FwdParams &p, const uint32_t *rowbits, int qt,
                                           int j) {
     if (qt >= p.T) return false;
     if (p.causal && j > qt) return false;
     if (p.mask == nullptr) return true;
-    return rowbits != nullptr ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
+    return p.T <= kMaskSmemTiles ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
 }
 
 // Bounded wait that ignores the abort flag: used only to drain copies and MMAs in flight.
@@ -131,14 +132,13 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(tmem_slot, L::kTmemCols);
         tmem_relinquish();
     }
-    uint32_t *mbits = nullptr;  // mask rows of qt0 and qt1, kMaskSmemWords words each
+    // mask rows of qt0 and qt1, kMaskSmemWords words each
+    uint32_t *const mrow0 = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+    uint32_t *const mrow1 = mrow0 + kMaskSmemWords;
     if (p.mask != nullptr && p.T <= kMaskSmemTiles) {
-        mbits = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
-        mask_bits_load(mbits, p.mask + static_cast<long>(qt0) * p.T, 1, p.T);
-        if (has1)
-            mask_bits_load(mbits + kMaskSmemWords, p.mask + static_cast<long>(qt1) * p.T, 1, p.T);
+        mask_bits_load(mrow0, p.mask + static_cast<long>(qt0) * p.T, 1, p.T);
+        if (has1) mask_bits_load(mrow1, p.mask + static_cast<long>(qt1) * p.T, 1, p.T);
     }
-    const uint32_t *mrow0 = mbits, *mrow1 = mbits != nullptr ? mbits + kMaskSmemWords : nullptr;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

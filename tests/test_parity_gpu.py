@@ -107,6 +107,25 @@ def test_block_sparse_small(cuda_lib, N, d, causal, seed):
     assert torch.all(grads[0][:, :, 128:256].cpu() == 0)
 
 
+@pytest.mark.parametrize("T", [4096, 4097])
+def test_block_mask_wider_than_shared_copy(cuda_lib, T):
+    # The kernels copy a mask row or column of up to 4096 tiles into shared memory as bits and
+    # read wider masks from global memory.  A mask of 2 x 2 diagonal super-blocks (and a lone
+    # last block when T is odd) splits the attention into independent problems of 256 rows
+    # (keys and queries alike), which the oracle solves one at a time.
+    N, d = T * BLOCK, 64
+    sb = torch.arange(T) // 2
+    mask = (sb[:, None] == sb[None, :]).to(torch.uint8).contiguous()
+    t = make_inputs(1, 1, N, d, torch.bfloat16, seed=41)
+    o, lse, grads = run_pair(cuda_lib, t, 0.125, False, mask)
+    for a in (0, 1400, 2 * ((T - 1) // 2)):
+        rows = slice(a * BLOCK, min(a + 2, T) * BLOCK)
+        sub = {x: t[x][0, 0, rows] for x in ("q", "k", "v", "do")}
+        ref = oracle.attention(sub["q"], sub["k"], sub["v"], 0.125, False, None, dout=sub["do"])
+        check_fwd(o[0, 0, rows], lse[0, 0, rows], ref, f"T={T} block {a}")
+        check_bwd([g[0, 0, rows] for g in grads], ref, f"T={T} block {a}")
+
+
 def expected_visits(BH, T, causal, mask):
     i = np.arange(T)
     live = np.ones((T, T), dtype=bool)
