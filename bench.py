@@ -10,6 +10,7 @@ FLOP convention (FlashAttention-2 reading notes, reproducibility section): forwa
 head, backward 2.5x that, both halved for causal attention.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+  python bench.py --sweep     # the pages' sequence-length sweep, one JSON line per shape
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, no data
 exchange); the time is the max over ranks and the value counts every rank's work.
@@ -718,6 +719,71 @@ def run_decode_reference(args, w):
     return 0
 
 
+# ------------------------------------------------------------------------------- sweep
+
+SWEEP_N = (512, 1024, 2048, 4096, 8192, 16384)
+
+
+def run_sweep(args):
+    """The kernel-throughput sweep of the FlashAttention-2 reading notes (benchmark section):
+    16k tokens per batch (B = 16384 / N), hidden size 2048 (H = 2048 / d), N from 512 to 16k,
+    head dimension 64 and 128, without and with the causal mask.  bf16 inputs drawn on the
+    device (iid N(0, 1), seeded); every call's inputs (201 MB or more) exceed the L2.  One JSON
+    line per shape: forward, backward (D pre-pass, dK/dV, dQ) and forward+backward TFLOP/s over
+    --steps calls after --warmup, CUDA events on the launching stream."""
+    from exact_attention_staged_gb300 import api
+    api.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2048)
+
+    def per_call_ms(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    for d in (64, 128):
+        for causal in (False, True):
+            for N in SWEEP_N:
+                B, H = 16384 // N, 2048 // d
+                q, k, v, do = (torch.randn(B, H, N, d, generator=gen, device=dev).to(torch.bfloat16)
+                               for _ in range(4))
+                scale = 1.0 / math.sqrt(d)
+                o = torch.empty_like(q)
+                lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                ws = torch.empty_like(lse)
+
+                def fwd():
+                    api.fwd(q, k, v, scale, causal, None, out=o, lse=lse)
+
+                def bwd():
+                    api.bwd(q, k, v, o, lse, do, scale, causal, None, dq=dq, dk=dk, dv=dv,
+                            workspace=ws)
+
+                fwd()
+                t_f = per_call_ms(fwd)
+                t_b = per_call_ms(bwd)
+                status = api.sync_status()
+                f = flops(B, H, N, d, causal)["fa_fwd_kernel"]
+                print(json.dumps({
+                    "sweep": "FlashAttention-2 kernel benchmark shapes", "B": B, "H": H, "N": N,
+                    "d": d, "causal": causal, "dtype": "bf16", "status": status,
+                    "fwd_ms": t_f, "bwd_ms": t_b,
+                    "fwd_tflops": f / t_f / 1e9, "bwd_tflops": 2.5 * f / t_b / 1e9,
+                    "fwd_bwd_tflops": 3.5 * f / (t_f + t_b) / 1e9}), flush=True)
+                del q, k, v, do, o, lse, dq, dk, dv, ws
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -727,9 +793,15 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(FP8_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the sequence-length sweep shapes instead (one line per shape)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.sweep:
+        if args.impl == "reference" or args.gpus != 1:
+            ap.error("--sweep runs our kernels on one GPU")
+        return run_sweep(args)
     if args.workload in FP8_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the e4m3 workload has no "
