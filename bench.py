@@ -63,6 +63,30 @@ def flops(B, H, N, d, causal, density=1.0):
             "fa_bwd_dkdv_kernel": 2.0 * f, "fa_bwd_dq_kernel": 0.5 * f}
 
 
+SMS = 152              # GB300 streaming multiprocessors
+EX2_PER_SM_CLK = 32    # ex2.approx results per SM per clock (probe kernel on the GB300)
+
+
+def mufu_bound(w, mask_cpu, fwd_ms, clocks):
+    """Secondary bound of the forward: its 2^x evaluations on the special-function units.  The
+    kernel computes one per element of every live 128 x 128 score tile (causal and block mask
+    as in the tile skipping); the peak is EX2_PER_SM_CLK x SMS x the median SM clock sampled
+    during the timed region (the maximum clock if none was sampled)."""
+    T = (w.N + 127) // 128
+    live = torch.ones(T, T, dtype=torch.bool)
+    if w.causal:
+        live = torch.tril(live)
+    if mask_cpu is not None:
+        live &= mask_cpu.bool()
+    exps = float(live.sum()) * 128 * 128 * w.B * w.H
+    mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = EX2_PER_SM_CLK * SMS * mhz * 1e6 / 1e12
+    achieved = exps / (fwd_ms / 1e3) / 1e12
+    return {"kernel": "fa_fwd_kernel", "exps_per_launch": exps, "achieved": achieved,
+            "peak": peak, "unit": "T ex2/s", "frac": achieved / peak,
+            "peak_kind": f"{EX2_PER_SM_CLK} per SM per clock x {SMS} SMs x {mhz:.0f} MHz"}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -338,7 +362,8 @@ def run_gpu(args, w):
     per_kernel = {}
     for i, n in enumerate(names):
         ms = [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
-        per_kernel[n] = {"ms": statistics.mean(ms),
+        per_kernel[n] = {"ms": statistics.mean(ms), "ms_median": statistics.median(ms),
+                         "ms_min": min(ms),
                          "tflops": f[n] / (statistics.mean(ms) / 1e3) / 1e12}
     fwd_ms = per_kernel["fa_fwd_kernel"]["ms"]
     bwd_ms = sum(per_kernel[n]["ms"] for n in names[1:])
@@ -459,6 +484,7 @@ def run_gpu(args, w):
         "frac_of_peak": value / world / peak,
         "kernels": per_kernel,
         "roofline": roofline,
+        "mufu": mufu_bound(w, mask_cpu, fwd_ms, clk.summary()),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
