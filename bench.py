@@ -219,6 +219,27 @@ def oracle_sample(w, inputs, head=0):
     return {"seconds": dt, "flops": f, "cores": oracle.num_threads()}
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, or implementer and part on Arm)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                k = k.strip()
+                if k in ("model name", "CPU implementer", "CPU part") and k not in fields:
+                    fields[k] = v.strip()
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return (f"{platform.machine()} (implementer {fields.get('CPU implementer', '?')}, "
+                f"part {fields['CPU part']})")
+    return platform.machine()
+
+
 def cpu_baseline(w, inputs, budget_s=10.0):
     """The oracle on whole heads of the workload, one after another, until ~budget_s."""
     secs, fl, heads, cores = 0.0, 0.0, 0, 1
@@ -229,6 +250,7 @@ def cpu_baseline(w, inputs, budget_s=10.0):
         cores = r["cores"]
         heads += 1
     return {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{heads} whole head(s) of the workload ({w.N} rows each), fp64 fwd+bwd, "
                       f"{secs:.1f} s"}
 
@@ -256,7 +278,7 @@ def run_reference(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.describe()},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
