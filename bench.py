@@ -622,8 +622,8 @@ def run_decode_gpu(args, w):
         oracle.decode(t["q"], t["k"], t["v"], w.scale, w.causal, t.get("kv_len"))
         secs = time.perf_counter() - t0
         cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
-               "kind": "oracle", "cpu": cpu_model(), "sample": f"the whole step ({w.B * w.H * w.Nq} rows), fp64 "
-                                           f"numpy, {secs:.1f} s"}
+               "kind": "oracle", "cpu": cpu_model(),
+               "sample": f"the whole step ({w.B * w.H * w.Nq} rows), fp64 numpy, {secs:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
@@ -760,8 +760,8 @@ def run_decode_reference(args, w):
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.describe()},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "cpu": cpu_model(),
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "cpu": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}), flush=True)
     return 0
