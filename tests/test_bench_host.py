@@ -79,3 +79,24 @@ def test_flop_convention():
 def test_warmup_floor_is_enforced():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_mufu_bound_counts_one_exponential_per_live_tile_element():
+    # brute force over the tile grid: causal keeps j <= i, the block mask keeps M[i][j] != 0
+    from exact_attention_staged_gb300.workloads import Workload
+    T = 5
+    mask = torch.tensor([[1, 0, 1, 1, 0], [0, 1, 0, 0, 1], [1, 1, 1, 0, 0], [0, 0, 1, 1, 1],
+                         [1, 0, 0, 1, 1]], dtype=torch.uint8)
+    for causal in (False, True):
+        for m in (None, mask):
+            w = Workload("t", 2, 3, T * 128 - 7, 64, "bf16", causal, 1)
+            live = sum(1 for i in range(T) for j in range(T)
+                       if (not causal or j <= i) and (m is None or m[i, j] != 0))
+            r = bench.mufu_bound(w, m, 1.0, {"sm_mhz": 1000.0, "sm_max_mhz": 2070.0})
+            assert r["exps_per_launch"] == live * 128 * 128 * 2 * 3
+            assert r["peak"] == pytest.approx(32 * 152 * 1000e6 / 1e12)
+            assert r["achieved"] == pytest.approx(r["exps_per_launch"] / 1e-3 / 1e12)
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
