@@ -137,9 +137,9 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         l_run[i] = 0.f;
     }
     const int cp = tid % kPairs, rs = tid / kPairs;
-    float acc[kRowsB][2];
+    float2 acc[kRowsB];  // this thread's two output columns of each of its rows
 #pragma unroll
-    for (int j = 0; j < kRowsB; ++j) acc[j][0] = acc[j][1] = 0.f;
+    for (int j = 0; j < kRowsB; ++j) acc[j] = make_float2(0.f, 0.f);
 
     for (int t = 0; t < ntiles; ++t) {
         const int stage = t % kStages;
@@ -150,39 +150,30 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         {  // A: partial dots of key `lane` over columns [warp * D/4, (warp + 1) * D/4)
             const uint8_t *krow =
                 smem + L::kKOff + stage * L::kTileBytes + lane * L::kRowBytes + warp * kQuarter * 2;
-            float dot[RPC];
+            float2 dot[RPC];  // even and odd columns summed apart (paired fp32 FMAs)
 #pragma unroll
-            for (int r = 0; r < RPC; ++r) dot[r] = 0.f;
+            for (int r = 0; r < RPC; ++r) dot[r] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c8 = 0; c8 < kQuarter / 8; ++c8) {
                 const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8 * 16);
-                const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
-                float kf[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack2<BF16>(w4[e]);
-                    kf[2 * e] = f.x;
-                    kf[2 * e + 1] = f.y;
-                }
+                const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y),
+                             k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
 #pragma unroll
                 for (int r = 0; r < RPC; ++r) {  // rows past nrows hold zeros
                     const float4 *qv =
                         reinterpret_cast<const float4 *>(qs + r * D + warp * kQuarter + c8 * 8);
                     const float4 a = qv[0], c = qv[1];
-                    float d = dot[r];
-                    d = fmaf(a.x, kf[0], d);
-                    d = fmaf(a.y, kf[1], d);
-                    d = fmaf(a.z, kf[2], d);
-                    d = fmaf(a.w, kf[3], d);
-                    d = fmaf(c.x, kf[4], d);
-                    d = fmaf(c.y, kf[5], d);
-                    d = fmaf(c.z, kf[6], d);
-                    d = fmaf(c.w, kf[7], d);
+                    float2 d = dot[r];
+                    d = ffma2(make_float2(a.x, a.y), k0, d);
+                    d = ffma2(make_float2(a.z, a.w), k1, d);
+                    d = ffma2(make_float2(c.x, c.y), k2, d);
+                    d = ffma2(make_float2(c.z, c.w), k3, d);
                     dot[r] = d;
                 }
             }
 #pragma unroll
-            for (int r = 0; r < RPC; ++r) part[(warp * RPC + r) * kKeys + lane] = dot[r];
+            for (int r = 0; r < RPC; ++r)
+                part[(warp * RPC + r) * kKeys + lane] = dot[r].x + dot[r].y;
         }
         __syncthreads();
         {  // A2: warp w owns rows w, w + 4, w + 8, w + 12
@@ -218,8 +209,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
                 const int r = rs + kRB * j;
                 if (r < nrows) {
                     const float a = alpha_s[r];
-                    acc[j][0] *= a;
-                    acc[j][1] *= a;
+                    acc[j] = fmul2(acc[j], make_float2(a, a));
                 }
             }
             if (rs < nrows) {
@@ -232,8 +222,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
                         const int r = rs + kRB * j;
                         if (RPC % kRB == 0 || r < RPC) {  // compile-time for whole row sets
                             const float pp = r < nrows ? ps[r * kKeys + key] : 0.f;
-                            acc[j][0] = fmaf(pp, vv.x, acc[j][0]);
-                            acc[j][1] = fmaf(pp, vv.y, acc[j][1]);
+                            acc[j] = ffma2(make_float2(pp, pp), vv, acc[j]);
                         }
                     }
                 }
@@ -261,12 +250,12 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         if (p.splits == 1) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
             reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.o) + grow * D)[cp] =
-                pack2<BF16>(acc[j][0] * inv, acc[j][1] * inv);
+                pack2<BF16>(acc[j].x * inv, acc[j].y * inv);
             if (cp == 0)
                 p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         } else {
             const long prow = static_cast<long>(split) * total_rows + grow;
-            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = make_float2(acc[j][0], acc[j][1]);
+            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = acc[j];
             if (cp == 0) reinterpret_cast<float2 *>(p.part_ml)[prow] = make_float2(m, l);
         }
     }
