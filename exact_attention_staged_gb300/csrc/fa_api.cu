@@ -83,6 +83,13 @@ int check_shape(int B, int H, int N, int d, int dtype, float scale) {
     return FA_OK;
 }
 
+// A block mask has T x T entries (T = ceil(N / 128)); the kernels index it with 32-bit
+// arithmetic, so T may not exceed 46340 (T^2 < 2^31, N <= 5931520).
+constexpr int kMaxMaskTiles = 46340;
+int check_mask(const uint8_t *mask, int N) {
+    return mask != nullptr && (N + 127) / 128 > kMaxMaskTiles ? FA_ERR_INVALID : FA_OK;
+}
+
 int check_ptrs(std::initializer_list<const void *> ptrs) {
     for (const void *p : ptrs)
         if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID;
@@ -197,6 +204,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
                const fa::DropSpec &drop, void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
     if (rc != FA_OK) return rc;
+    rc = check_mask(mask, N);
+    if (rc != FA_OK) return rc;
     rc = check_heads(H, Hkv);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, o, lse});
@@ -233,6 +242,8 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
                int causal, const uint8_t *mask, const fa::DropSpec &drop, fa::Maps *maps,
                fa::BwdParams *p) {
     int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_mask(mask, N);
     if (rc != FA_OK) return rc;
     rc = check_heads(H, Hkv);
     if (rc != FA_OK) return rc;
@@ -358,6 +369,8 @@ int bwd_entry(const void *q, const void *k, const void *v, const void *o, const 
               float scale, int causal, const uint8_t *block_mask, const fa::DropSpec &drop,
               void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_mask(block_mask, N);
     if (rc != FA_OK) return rc;
     rc = check_heads(H, H_kv);
     if (rc != FA_OK) return rc;
@@ -543,6 +556,8 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
                float descale_v, int causal, const uint8_t *block_mask, void *workspace,
                size_t workspace_bytes, void *stream) {
     int rc = check_shape(B, H, N, d, FA_BF16, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_mask(block_mask, N);
     if (rc != FA_OK) return rc;
     rc = check_heads(H, H_kv);
     if (rc != FA_OK) return rc;

@@ -614,7 +614,7 @@ __device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
 }
 // The same after every lane's prior tensor-memory stores have completed.
 __device__ __forceinline__ void mbar_arrive_warp_after_st(uint64_t *bar) {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tmem_wait_st();
     mbar_arrive_warp(bar);
 }
 

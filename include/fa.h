@@ -17,7 +17,8 @@
  *            (b, h); entry (i, j) != 0 keeps the 128 x 128 score block of query rows
  *            [128 i, 128 i + 128) and key rows [128 j, 128 j + 128).  With both, a score is kept
  *            only if both keep it.  A query row whose every key is masked gets O = 0,
- *            LSE = -inf and zero gradients.
+ *            LSE = -inf and zero gradients.  With a block mask T may not exceed 46340
+ *            (N <= 5931520; T x T stays below 2^31), else FA_ERR_INVALID.
  *  Ownership The caller owns every buffer.  The library allocates no device memory on any
  *            call; it keeps one device status word per device, created on first use.
  *  Streams   Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy default

@@ -70,6 +70,11 @@ def test_host_validation_rejects_before_launch(lib):
     p = ctypes.c_void_p(16)
     assert lib.fa_fwd_blocksparse(p, p, p, p, p, 1, 1, 128, 64, 1, 0.125, 0, None,
                                   None) == api.FA_ERR_INVALID  # block mask required
+    # a block mask of more than 46340 x 46340 tiles (T^2 >= 2^31) is refused
+    assert lib.fa_fwd_blocksparse(p, p, p, p, p, 1, 1, 46341 * 128, 64, 1, 0.125, 0, p,
+                                  None) == api.FA_ERR_INVALID
+    assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1 << 30, 1, 1, 46341 * 128, 64, 1, 0.125, 0,
+                      p, None) == api.FA_ERR_INVALID
     assert lib.fa_bwd(p, p, p, p, p, p, p, p, p, p, 0, 1, 1, 128, 64, 1, 0.125, 0, None,
                       None) == api.FA_ERR_INVALID  # workspace too small
     assert lib.fa_debug_set_fault(5) == api.FA_ERR_INVALID
