@@ -55,14 +55,6 @@ __device__ __forceinline__ void next_unit(const BwdParams &p, const uint32_t *bi
     }
 }
 
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(a, parity)) {
-        if (global_timer_ns() - t0 > ctl.wait_limit_ns) return;
-    }
-}
-
 // LSE in log2 units for the exponent; rows that are out of range or fully masked (LSE = -inf)
 // get +inf so that every recomputed probability of theirs is exactly 0.
 __device__ __forceinline__ float lse_log2(const BwdParams &p, int bh, int row) {

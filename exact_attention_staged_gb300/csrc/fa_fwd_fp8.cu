@@ -45,29 +45,6 @@ struct Fp8Layout {
     static constexpr int kThreads = 384;
 };
 
-__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    const uint32_t a = smem_u32(p);
-    return p + ((1024u - (a & 1023u)) & 1023u);
-}
-
-// rowbits: where the query tile's mask row is kept as bits in shared memory when the mask is
-// at most kMaskSmemTiles wide; wider masks are read from global memory
-__device__ __forceinline__ bool tile_live(const Fp8FwdParams &p, const uint32_t *rowbits, int qt,
-                                          int j) {
-    if (qt >= p.T) return false;
-    if (p.causal && j > qt) return false;
-    if (p.mask == nullptr) return true;
-    return p.T <= kMaskSmemTiles ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(a, parity)) {
-        if (global_timer_ns() - t0 > ctl.wait_limit_ns) return;
-    }
-}
-
 // Q and K tiles: 128 rows of d bytes (128-byte swizzle at d = 128, 64-byte at d = 64).
 template <int D>
 __device__ __forceinline__ SDesc qk_desc(uint32_t saddr) {

@@ -39,6 +39,17 @@ __device__ __forceinline__ bool mask_bit(const uint32_t *bits, int i) {
     return ((bits[i >> 5] >> (i & 31)) & 1u) != 0;
 }
 
+// Forward kernels (bf16/fp16 and e4m3 parameter blocks alike): is key tile j live for query tile
+// qt?  rowbits: where the query tile's mask row is kept as bits in shared memory when the mask
+// is at most kMaskSmemTiles wide; wider masks are read from global memory.
+template <class Params>
+__device__ __forceinline__ bool tile_live(const Params &p, const uint32_t *rowbits, int qt, int j) {
+    if (qt >= p.T) return false;
+    if (p.causal && j > qt) return false;
+    if (p.mask == nullptr) return true;
+    return p.T <= kMaskSmemTiles ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
+}
+
 // CTA order: heads are taken in groups of `group` so that the tiles streamed by the CTAs that
 // run at the same time (K/V of the forward, Q/dO of dK/dV, K/V of dQ) stay within a slice of
 // L2; inside a group the work unit (query-tile pair or tile) advances slowest, longest first.

@@ -114,6 +114,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
+// Bounded wait that ignores the abort flag: used only to drain copies and MMAs in flight before
+// a CTA that gave up releases its shared and tensor memory.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (global_timer_ns() - t0 > ctl.wait_limit_ns) return;
+    }
+}
+
+// First 1024-byte-aligned address at or after p (the 128-byte swizzle's pattern repeats every
+// 1024 bytes, so swizzled tiles start on such a boundary).
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    const uint32_t a = smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
 // Warp-uniform form of mbar_wait for warps that go on to warp-collective operations
 // (tcgen05.ld/st, vote): either every lane of the warp proceeds or none does.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const Ctl &ctl,
