@@ -287,6 +287,33 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------------------- GPU arm
 
+def graph_replay_ms(step, steps, warmup):
+    """The step captured once into a CUDA graph and replayed: the host's per-call work (argument
+    checks, tensor maps, launches through the C ABI) happens at capture only, so a launch-bound
+    shape runs at the GPU's pace.  Returns (ms per step, None) or (None, why not)."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=side):
+            step()
+        torch.cuda.synchronize()
+    except Exception as exc:  # capture refused: report it, keep the eager numbers
+        torch.cuda.synchronize()
+        return None, f"capture failed: {type(exc).__name__}: {str(exc)[:120]}"
+    cur = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(cur)
+    for _ in range(steps):
+        g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, None
+
+
 def run_gpu(args, w):
     from exact_attention_staged_gb300 import api
     world, rank, local = dist_setup()
@@ -477,6 +504,17 @@ def run_gpu(args, w):
         raise RuntimeError("device status reported an error in the end-to-end loop")
     e2e_value = world * step_flops * e2e_steps / (e2e_ms / 1e3) / 1e12
 
+    # ---- the same step replayed from a CUDA graph (beside the eager timing, not instead of it)
+    g_ms, g_why = graph_replay_ms(step, args.steps, args.warmup)
+    if g_ms is not None:
+        g_ms = dist_max(g_ms, world, dev)
+        if api.sync_status() != 0:
+            raise RuntimeError("device status reported an error in the graph replays")
+        graph = {"value": world * step_flops / (g_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                 "ms_per_step": g_ms, "steps": args.steps}
+    else:
+        graph = {"unavailable": g_why}
+
     launches_per_step = 4  # fwd, D, dK/dV, dQ (+ the group reduce when dK/dV is split)
     if gqa and api.gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d) > \
             api.workspace_bytes(w.B, w.H, w.N, w.d):
@@ -513,6 +551,7 @@ def run_gpu(args, w):
                 "copies": "pinned host buffers; each step's copies overlap the neighbouring "
                           "steps' compute (two device buffer sets, separate copy streams)"},
         "gpu_launches": launches_per_step * args.steps,
+        "graph": graph,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
