@@ -70,6 +70,9 @@ class FAError(RuntimeError):
 def load(path: str = LIB_PATH):
     """Load libfa.so (built by ``exact_attention_staged_gb300.build``); raise if absent."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is None:
             if not os.path.exists(path):
@@ -110,12 +113,20 @@ def _dev(t: Optional[torch.Tensor], name: str, like: Optional[torch.Tensor] = No
         raise ValueError(f"{name} must be contiguous")
     if like is not None and (t.shape != like.shape or t.dtype != like.dtype):
         raise ValueError(f"{name} must match q in shape and dtype")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()  # ctypes passes the int as the c_void_p argument
 
 
-def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream: Optional[torch.cuda.Stream], like: Optional[torch.Tensor] = None) -> int:
+    """The CUDA stream handle to launch on: `stream`, else the current stream of the tensor's
+    device (read as a raw handle: no Stream object is built on the per-call path)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and like is not None:
+        return _raw_stream(like.device.index)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _shape(q: torch.Tensor):
@@ -139,11 +150,11 @@ def fwd(q, k, v, scale: Optional[float] = None, causal: bool = False, block_mask
     args = [_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q), _dev(out, "out", q), _dev(lse, "lse"),
             B, H, N, d, _dtype_code(q), float(scale), int(bool(causal))]
     if block_mask is None:
-        _check(lib.fa_fwd(*args, _stream(stream)), "fa_fwd")
+        _check(lib.fa_fwd(*args, _stream(stream, q)), "fa_fwd")
     else:
         if block_mask.dtype != torch.uint8:
             raise TypeError("block_mask must be uint8")
-        _check(lib.fa_fwd_blocksparse(*args, _dev(block_mask, "block_mask"), _stream(stream)),
+        _check(lib.fa_fwd_blocksparse(*args, _dev(block_mask, "block_mask"), _stream(stream, q)),
                "fa_fwd_blocksparse")
     return out, lse
 
@@ -172,14 +183,14 @@ def bwd(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool = Fal
                       _dev(dout, "dout", q), _dev(lse, "lse"), _dev(dq, "dq", q),
                       _dev(dk, "dk", q), _dev(dv, "dv", q), _dev(workspace, "workspace"),
                       nbytes, B, H, N, d, _dtype_code(q), float(scale), int(bool(causal)),
-                      mask_ptr, _stream(stream)), "fa_bwd")
+                      mask_ptr, _stream(stream, q)), "fa_bwd")
     return dq, dk, dv
 
 
 def bwd_preprocess(o, dout, delta, stream=None):
     B, H, N, d = _shape(o)
     _check(load().fa_bwd_preprocess(_dev(o, "o"), _dev(dout, "dout", o), _dev(delta, "delta"),
-                                    B, H, N, d, _dtype_code(o), _stream(stream)),
+                                    B, H, N, d, _dtype_code(o), _stream(stream, o)),
            "fa_bwd_preprocess")
     return delta
 
@@ -192,7 +203,7 @@ def bwd_dkdv(q, k, v, dout, lse, delta, dk, dv, scale=None, causal=False, block_
     _check(load().fa_bwd_dkdv(_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q),
                               _dev(dout, "dout", q), _dev(lse, "lse"), _dev(delta, "delta"),
                               _dev(dk, "dk", q), _dev(dv, "dv", q), B, H, N, d, _dtype_code(q),
-                              float(scale), int(bool(causal)), mask_ptr, _stream(stream)),
+                              float(scale), int(bool(causal)), mask_ptr, _stream(stream, q)),
            "fa_bwd_dkdv")
     return dk, dv
 
@@ -205,7 +216,7 @@ def bwd_dq(q, k, v, dout, lse, delta, dq, scale=None, causal=False, block_mask=N
     _check(load().fa_bwd_dq(_dev(q, "q"), _dev(k, "k", q), _dev(v, "v", q),
                             _dev(dout, "dout", q), _dev(lse, "lse"), _dev(delta, "delta"),
                             _dev(dq, "dq", q), B, H, N, d, _dtype_code(q), float(scale),
-                            int(bool(causal)), mask_ptr, _stream(stream)), "fa_bwd_dq")
+                            int(bool(causal)), mask_ptr, _stream(stream, q)), "fa_bwd_dq")
     return dq
 
 
@@ -235,7 +246,7 @@ def fwd_gqa(q, k, v, scale: Optional[float] = None, causal: bool = False, block_
     mask_ptr = None if block_mask is None else _dev(block_mask, "block_mask")
     _check(lib.fa_fwd_gqa(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
                           _dev(lse, "lse"), B, H, Hkv, N, d, _dtype_code(q), float(scale),
-                          int(bool(causal)), mask_ptr, _stream(stream)), "fa_fwd_gqa")
+                          int(bool(causal)), mask_ptr, _stream(stream, q)), "fa_fwd_gqa")
     return out, lse
 
 
@@ -267,7 +278,7 @@ def fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
                           _dev(lse, "lse"), B, H, Hkv, N, d, float(scale), float(descale_q),
                           float(descale_k), float(descale_v), int(bool(causal)), mask_ptr,
                           _dev(workspace, "workspace"),
-                          workspace.numel() * workspace.element_size(), _stream(stream)),
+                          workspace.numel() * workspace.element_size(), _stream(stream, q)),
            "fa_fwd_fp8")
     return out, lse
 
@@ -298,7 +309,7 @@ def bwd_gqa(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool =
                           _dev(dout, "dout", q), _dev(lse, "lse"), _dev(dq, "dq", q),
                           _dev(dk, "dk", k), _dev(dv, "dv", k), _dev(workspace, "workspace"),
                           nbytes, B, H, Hkv, N, d, _dtype_code(q), float(scale),
-                          int(bool(causal)), mask_ptr, _stream(stream)), "fa_bwd_gqa")
+                          int(bool(causal)), mask_ptr, _stream(stream, q)), "fa_bwd_gqa")
     return dq, dk, dv
 
 
@@ -332,7 +343,7 @@ def decode(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_len=
     _check(lib.fa_decode(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
                          _dev(lse, "lse"), None if kv_len is None else _dev(kv_len, "kv_len"),
                          B, H, Hkv, Nq, Nk, d, _dtype_code(q), float(scale), int(bool(causal)),
-                         ws, nbytes, _stream(stream)), "fa_decode")
+                         ws, nbytes, _stream(stream, q)), "fa_decode")
     return out, lse
 
 
@@ -350,7 +361,7 @@ def fwd_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0,
     _check(lib.fa_fwd_dropout(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", q),
                               _dev(lse, "lse"), B, H, Hkv, N, d, _dtype_code(q), float(scale),
                               int(bool(causal)), mask_ptr, float(p_drop), int(seed), int(offset),
-                              _stream(stream)), "fa_fwd_dropout")
+                              _stream(stream, q)), "fa_fwd_dropout")
     return out, lse
 
 
@@ -376,7 +387,7 @@ def bwd_dropout(q, k, v, o, lse, dout, p_drop: float, seed: int, offset: int = 0
                               _dev(dk, "dk", k), _dev(dv, "dv", k), _dev(workspace, "workspace"),
                               nbytes, B, H, Hkv, N, d, _dtype_code(q), float(scale),
                               int(bool(causal)), mask_ptr, float(p_drop), int(seed), int(offset),
-                              _stream(stream)), "fa_bwd_dropout")
+                              _stream(stream, q)), "fa_bwd_dropout")
     return dq, dk, dv
 
 
