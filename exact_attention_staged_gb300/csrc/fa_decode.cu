@@ -20,9 +20,13 @@
 //       scale * log2 e);
 //   A2  warp w owns rows w, w+4, ...: sums the four quarters, masks, takes the tile max with
 //       shuffles, P = 2^(s - m), l = alpha l + sum P;
-//   B   every thread owns two output columns of some rows: O = alpha O + P V.
-// With one key range the CTA writes O and LSE; otherwise it writes (m, l, unnormalised O) and
-// fa_decode_combine_kernel merges the ranges in order (deterministic).
+//   B   every thread owns two output columns of every row and a fixed share of the tile's keys
+//       (key group): O_g = alpha O_g + P V over its keys, P read four keys per shared load, so
+//       each V element and each probability is read from shared memory once per tile.
+// The key groups' partial outputs share the row statistics (alpha is per row and tile), so they
+// are summed once, after the last tile.  With one key range the CTA then writes O and LSE;
+// otherwise it writes (m, l, unnormalised O) and fa_decode_combine_kernel merges the ranges in
+// order (deterministic).
 #include "fa_internal.h"
 
 #include <cmath>
@@ -69,8 +73,12 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     using L = DecLayout<D, RPC>;
     using T = elem_t<BF16>;
     constexpr int kPairs = D / 2;                 // column pairs of O
-    constexpr int kRB = kThreads / kPairs;        // row sets in phase B (2 for d=128, 4 for 64)
-    constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in phase B
+    constexpr int kRB = kThreads / kPairs;        // key groups in phase B (2 for d=128, 4 for 64)
+    constexpr int kKeysB = kKeys / kRB;           // keys per group and tile (16 or 8)
+    constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in the final merge and store
+    static_assert(kKeysB % 4 == 0, "probabilities are read four keys at a time");
+    static_assert(kRB * RPC * D * 4 <= 2 * kStages * L::kTileBytes,
+                  "the merge buffer reuses the K/V ring");
     constexpr int kQuarter = D / 4;               // columns per warp in phase A
     constexpr int kChunks = D * 2 / 16;           // 16-byte chunks per K/V row
     constexpr int kRowsA2 = (RPC + 3) / 4;        // rows per warp in phase A2
@@ -136,10 +144,10 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         m_run[i] = -INFINITY;
         l_run[i] = 0.f;
     }
-    const int cp = tid % kPairs, rs = tid / kPairs;
-    float2 acc[kRowsB];  // this thread's two output columns of each of its rows
+    const int cp = tid % kPairs, rs = tid / kPairs;  // column pair; key group (phase B)
+    float2 acc[RPC];  // this thread's two output columns of every row, over its key group
 #pragma unroll
-    for (int j = 0; j < kRowsB; ++j) acc[j] = make_float2(0.f, 0.f);
+    for (int r = 0; r < RPC; ++r) acc[r] = make_float2(0.f, 0.f);
 
     for (int t = 0; t < ntiles; ++t) {
         const int stage = t % kStages;
@@ -202,28 +210,34 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
             }
         }
         __syncthreads();
-        {  // B: O = alpha O + P V for this thread's two columns
-            const uint8_t *vcol = smem + L::kVOff + stage * L::kTileBytes + cp * 4;
+        {  // B: O_g = alpha O_g + P V over this thread's key group, two columns, every row
+            const uint8_t *vcol = smem + L::kVOff + stage * L::kTileBytes +
+                                  rs * kKeysB * L::kRowBytes + cp * 4;
+            const float *pg = ps + rs * kKeysB;
 #pragma unroll
-            for (int j = 0; j < kRowsB; ++j) {
-                const int r = rs + kRB * j;
+            for (int r = 0; r < RPC; ++r) {
                 if (r < nrows) {
                     const float a = alpha_s[r];
-                    acc[j] = fmul2(acc[j], make_float2(a, a));
+                    acc[r] = fmul2(acc[r], make_float2(a, a));
                 }
             }
-            if (rs < nrows) {
-#pragma unroll 8
-                for (int key = 0; key < kKeys; ++key) {
-                    const float2 vv = unpack2<BF16>(
-                        *reinterpret_cast<const uint32_t *>(vcol + key * L::kRowBytes));
 #pragma unroll
-                    for (int j = 0; j < kRowsB; ++j) {
-                        const int r = rs + kRB * j;
-                        if (RPC % kRB == 0 || r < RPC) {  // compile-time for whole row sets
-                            const float pp = r < nrows ? ps[r * kKeys + key] : 0.f;
-                            acc[j] = ffma2(make_float2(pp, pp), vv, acc[j]);
-                        }
+            for (int k4 = 0; k4 < kKeysB; k4 += 4) {
+                float2 vv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    vv[u] = unpack2<BF16>(
+                        *reinterpret_cast<const uint32_t *>(vcol + (k4 + u) * L::kRowBytes));
+#pragma unroll
+                for (int r = 0; r < RPC; ++r) {
+                    if (r < nrows) {  // rows past nrows have no probabilities this tile
+                        const float4 p4 = *reinterpret_cast<const float4 *>(pg + r * kKeys + k4);
+                        float2 o = acc[r];
+                        o = ffma2(make_float2(p4.x, p4.x), vv[0], o);
+                        o = ffma2(make_float2(p4.y, p4.y), vv[1], o);
+                        o = ffma2(make_float2(p4.z, p4.z), vv[2], o);
+                        o = ffma2(make_float2(p4.w, p4.w), vv[3], o);
+                        acc[r] = o;
                     }
                 }
             }
@@ -239,23 +253,36 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
             l_s[r] = l_run[i];
         }
     }
+    __syncthreads();  // every thread is past its last read of the K/V ring
+    // merge of the key groups: group g's partial output of row r at red[(g * RPC + r) * D]
+    float *red = reinterpret_cast<float *>(smem + L::kKOff);
+#pragma unroll
+    for (int r = 0; r < RPC; ++r)
+        if (r < nrows) reinterpret_cast<float2 *>(red + (rs * RPC + r) * D)[cp] = acc[r];
     __syncthreads();
     const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
 #pragma unroll
     for (int j = 0; j < kRowsB; ++j) {
         const int r = rs + kRB * j;
         if (r >= nrows) continue;
+        float2 o = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < kRB; ++g) {  // fixed order: deterministic
+            const float2 x = reinterpret_cast<const float2 *>(red + (g * RPC + r) * D)[cp];
+            o.x += x.x;
+            o.y += x.y;
+        }
         const long grow = grow0 + r;
         const float m = m_s[r], l = l_s[r];
         if (p.splits == 1) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
             reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.o) + grow * D)[cp] =
-                pack2<BF16>(acc[j].x * inv, acc[j].y * inv);
+                pack2<BF16>(o.x * inv, o.y * inv);
             if (cp == 0)
                 p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         } else {
             const long prow = static_cast<long>(split) * total_rows + grow;
-            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = acc[j];
+            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = o;
             if (cp == 0) reinterpret_cast<float2 *>(p.part_ml)[prow] = make_float2(m, l);
         }
     }
