@@ -300,8 +300,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     if (row >= total_rows) return;
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
     // the ranges' statistics 32 at a time, lane s holding range s: M, the weights 2^(m_s - M)
-    // and l = sum w_s l_s by shuffles; then O = sum w_s O_s with every range's load issued
-    // before its use (the weights come from the lanes)
+    // and l = sum w_s l_s by shuffles; then O = sum w_s O_s (the weights come from the lanes)
     float M = -INFINITY;
     for (int s0 = 0; s0 < p.splits; s0 += 32) {
         const int s = s0 + lane;
@@ -326,13 +325,26 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
         lsum += lw;
+        // eight ranges' partial outputs loaded before any is used, so their latencies overlap;
+        // a range past the last one reads as zero with weight zero (its lane's w is 0)
         const int n = min(32, p.splits - s0);
-        for (int i = 0; i < n; ++i) {
-            const float wi = __shfl_sync(0xffffffffu, w, i);
-            const float *src = p.part_o + (static_cast<long>(s0 + i) * total_rows + row) * D +
-                               lane * kCols;
+        for (int i0 = 0; i0 < n; i0 += 8) {
+            float x[8][kCols];
 #pragma unroll
-            for (int c = 0; c < kCols; ++c) acc[c] = fmaf(wi, src[c], acc[c]);
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u;
+                const float *src = p.part_o +
+                                   (static_cast<long>(s0 + min(i, n - 1)) * total_rows + row) * D +
+                                   lane * kCols;
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) x[u][c] = i < n ? src[c] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float wi = __shfl_sync(0xffffffffu, w, i0 + u);
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) acc[c] = fmaf(wi, x[u][c], acc[c]);
+            }
         }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
