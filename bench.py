@@ -51,6 +51,8 @@ KERNEL_SOURCES = {
     "fa_bwd_dkdv_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
     "fa_bwd_dq_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
     "fa_bwd_preprocess_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
+    "fa_decode_kernel": (_CSRC + "fa_decode.cu",) + _SHARED,
+    "fa_decode_combine_kernel": (_CSRC + "fa_decode.cu",) + _SHARED,
 }
 
 
@@ -577,6 +579,14 @@ def decode_work(w, t):
     return fl, nbytes
 
 
+def decode_traffic(workload, nws):
+    """DRAM bytes of one decode step (the decode kernel, plus the merge when the key range is
+    split) from the committed ncu summary, or None if either kernel changed since."""
+    kernels = ["fa_decode_kernel"] + (["fa_decode_combine_kernel"] if nws else [])
+    per = [ncu_traffic(k, workload) for k in kernels]
+    return None if any(x is None for x in per) else sum(per)
+
+
 def run_decode_gpu(args, w):
     from exact_attention_staged_gb300 import api
     world, rank, local = dist_setup()
@@ -621,7 +631,7 @@ def run_decode_gpu(args, w):
     roofline = {"bound": "hbm", "kernel": "fa_decode_kernel" +
                 ("" if nws == 0 else " + fa_decode_combine_kernel"),
                 "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                "frac": gbs / peaks["hbm_gbs"], "traffic": decode_traffic(w.name, nws),
                 "algorithmic_bytes": nbytes,
                 "peak_kind": f"HBM copy ({peaks['source']})"}
 

@@ -100,3 +100,24 @@ def test_mufu_bound_counts_one_exponential_per_live_tile_element():
 
 def test_cpu_model_is_named():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_stored_traffic_is_used_only_while_the_kernel_sources_match(monkeypatch):
+    # every stored record names a kernel bench.py knows and carries its sources' hash
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        stored = json.load(f)
+    for workload, kernels in stored.items():
+        for kernel, rec in kernels.items():
+            assert kernel in bench.KERNEL_SOURCES, kernel
+            assert rec["dram_bytes_per_launch"] == rec["dram_read"] + rec["dram_write"]
+            assert rec["command"].startswith("ncu ") and "--clock-control none" in rec["command"]
+    # the decode step's figure is the decode kernel plus the merge, the merge only when split
+    one = bench.ncu_traffic("fa_decode_kernel", "decode_gqa_d128_kv8k")
+    merge = bench.ncu_traffic("fa_decode_combine_kernel", "decode_gqa_d128_kv8k")
+    if one is not None and merge is not None:
+        assert bench.decode_traffic("decode_gqa_d128_kv8k", 1) == one + merge
+        assert bench.decode_traffic("decode_gqa_d128_kv8k", 0) == one
+    # a changed source (here: the hash taken over another file) voids the stored figure
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "fa_decode_kernel", ("bench.py",))
+    assert bench.ncu_traffic("fa_decode_kernel", "decode_gqa_d128_kv8k") is None
+    assert bench.decode_traffic("decode_gqa_d128_kv8k", 1) is None
