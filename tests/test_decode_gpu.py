@@ -32,6 +32,8 @@ CASES = [  # B, H, H_kv, Nq, Nk, d, causal, ragged
     (2, 4, 1, 4, 777, 128, True, True),     # MQA, 4 new rows, end-aligned causal: 16 rows
     (1, 32, 1, 1, 5000, 64, False, False),  # 32 rows per K/V head: two row groups
     (2, 6, 3, 3, 4096, 64, True, False),
+    (2, 4, 2, 1, 513, 128, False, False),   # 2 rows per K/V head
+    (1, 8, 1, 1, 1500, 128, True, True),    # 8 rows per K/V head at d = 128
 ]
 
 
