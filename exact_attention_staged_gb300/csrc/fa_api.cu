@@ -388,13 +388,14 @@ int bwd_entry(const void *q, const void *k, const void *v, const void *o, const 
                    scale, causal, block_mask, drop, stream);
 }
 
-// Decode key ranges: as many per (K/V head, row group) as give about twelve 128-thread CTAs per
-// SM of a 152-SM GB300, but no range shorter than 256 keys; ranges are multiples of the
-// kernel's 32-key tile.  A CTA works through its tiles with block-wide barriers, so more CTAs
-// per SM, not a deeper prefetch ring, keep the memory system busy (measured on the 8k-cache
-// workload: 3 CTAs per SM reach 0.49 of the copy bandwidth, 12 reach 0.57; a 5-stage ring was
-// slower).
-constexpr long kDecodeWaveCtas = 12 * 152;
+// Decode key ranges: as many per (K/V head, row group) as give about 28 128-thread CTAs per SM
+// of a 152-SM GB300 (four waves of seven resident CTAs), but no range shorter than 256 keys;
+// ranges are multiples of 32 keys (two of the kernel's 16-key tiles).  A CTA works through its
+// tiles with block-wide barriers, so more resident CTAs, not a deeper prefetch ring, keep the
+// memory system busy (measured on the 8k-cache workload: 3 CTAs per SM of the earlier 32-key
+// kernel reached 0.49 of the copy bandwidth, 12 reached 0.57, a 5-stage ring was slower; the
+// 16-key kernel at 7, 14, 21 and 28 CTAs per SM: 0.120, 0.119, 0.120 and 0.117 ms per step).
+constexpr long kDecodeWaveCtas = 28 * 152;
 struct DecodeSplit {
     int splits, chunk, row_groups;
 };

@@ -11,15 +11,16 @@
 // l = e^(m1-m) l1 + e^(m2-m) l2, and the outputs weighted the same way).
 //
 // GB300 mapping: no tensor cores (one to sixteen rows per key: 4 to 64 FLOP per 16-bit K/V
-// element pair, far below what would make the MMA pipe the limit); 128 threads per CTA, a few
-// CTAs per SM.  K and V tiles of 32 keys stream through a two-stage cp.async ring into
-// padded shared-memory rows (272 or 144 bytes, so 16-byte reads of 8 consecutive rows hit
-// distinct banks).  Per tile:
-//   A   every warp takes a quarter of d, every lane one key: partial dot products of that key
-//       with all rows (query rows broadcast from shared memory, fp32, pre-scaled by
-//       scale * log2 e);
+// element pair, far below what would make the MMA pipe the limit); 128 threads per CTA, seven
+// CTAs per SM at up to four rows (each CTA's tile loop is a chain of barriers and shuffles, so
+// resident CTAs set the rate).  K and V tiles of 16 keys stream through a three-stage cp.async
+// ring (K rows padded to 272 or 144 bytes, so 16-byte reads of 8 consecutive rows hit distinct
+// banks).  Per tile:
+//   A   every warp takes a quarter of d, every lane one key and half of that quarter: partial
+//       dot products of that key with all rows (query rows broadcast from shared memory, fp32,
+//       pre-scaled by scale * log2 e), the two halves summed by one shuffle;
 //   A2  warp w owns rows w, w+4, ...: sums the four quarters, masks, takes the tile max with
-//       shuffles, P = 2^(s - m), l = alpha l + sum P;
+//       shuffles over 16 lanes, P = 2^(s - m), l = alpha l + sum P;
 //   B   every thread owns two output columns of every row and a fixed share of the tile's keys
 //       (key group): O_g = alpha O_g + P V over its keys, P read four keys per shared load, so
 //       each V element and each probability is read from shared memory once per tile.
@@ -36,18 +37,22 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kKeys = 32;     // keys per shared-memory tile
+constexpr int kKeys = 16;     // keys per shared-memory tile (lane = key and column half)
 constexpr int kStages = 3;    // K/V tiles in the cp.async ring (two in flight while one is used)
 
 template <int D, int RPC>
 struct DecLayout {
-    static constexpr int kRowBytes = D * 2 + 16;  // padded 16-bit K or V row
-    static constexpr int kTileBytes = kKeys * kRowBytes;
+    // K rows padded by 16 bytes (phase A reads 16 bytes of 8 consecutive rows at once); V rows
+    // not (phase B reads 128 contiguous bytes of one row per warp)
+    static constexpr int kKRowBytes = D * 2 + 16;
+    static constexpr int kVRowBytes = D * 2;
+    static constexpr int kKTileBytes = kKeys * kKRowBytes;
+    static constexpr int kVTileBytes = kKeys * kVRowBytes;
     static constexpr int kQOff = 0;                                 // float [RPC][D]
     static constexpr int kKOff = kQOff + RPC * D * 4;               // kStages tiles
-    static constexpr int kVOff = kKOff + kStages * kTileBytes;      // kStages tiles
-    static constexpr int kPartOff = kVOff + kStages * kTileBytes;   // float [4][RPC][32]
-    static constexpr int kPOff = kPartOff + 4 * RPC * kKeys * 4;    // float [RPC][32]
+    static constexpr int kVOff = kKOff + kStages * kKTileBytes;     // kStages tiles
+    static constexpr int kPartOff = kVOff + kStages * kVTileBytes;  // float [4][RPC][kKeys]
+    static constexpr int kPOff = kPartOff + 4 * RPC * kKeys * 4;    // float [RPC][kKeys]
     static constexpr int kStatOff = kPOff + RPC * kKeys * 4;        // alpha, m, l [RPC] each
     static constexpr int kBytes = kStatOff + 3 * RPC * 4;
 };
@@ -55,15 +60,16 @@ struct DecLayout {
 template <bool BF16>
 using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
-__device__ __forceinline__ float warp_max(float v) {
+// reductions over each 16-lane half of a warp (both halves hold the same 16 keys)
+__device__ __forceinline__ float half_max(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+__device__ __forceinline__ float half_sum(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
@@ -77,9 +83,11 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     constexpr int kKeysB = kKeys / kRB;           // keys per group and tile (16 or 8)
     constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in the final merge and store
     static_assert(kKeysB % 4 == 0, "probabilities are read four keys at a time");
-    static_assert(kRB * RPC * D * 4 <= 2 * kStages * L::kTileBytes,
-                  "the merge buffer reuses the K/V ring");
+    static_assert(kRB * RPC * D * 4 <= L::kPOff,
+                  "the merge buffer reuses the query rows, the K/V ring and the partial dots");
     constexpr int kQuarter = D / 4;               // columns per warp in phase A
+    constexpr int kHalf = kQuarter / 2;           // columns per lane in phase A (16 or 8)
+    static_assert(kKeys == 16, "phase A maps a warp's lanes to 16 keys x 2 column halves");
     constexpr int kChunks = D * 2 / 16;           // 16-byte chunks per K/V row
     constexpr int kRowsA2 = (RPC + 3) / 4;        // rows per warp in phase A2
     extern __shared__ __align__(16) uint8_t smem[];
@@ -105,6 +113,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     const int k_end = min(k_begin + p.chunk, len);
     const int ntiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kl = lane & (kKeys - 1), half = lane >> 4;  // phase A / A2: key, column half
     // CTA row r is group row r0 + r: query head kvh * rep + (r0 + r) / Nq, new row (r0 + r) % Nq,
     // i.e. global row ((b * H + h) * Nq + i) = kvh * rows + r0 + r
     const long grow0 = static_cast<long>(kvh) * p.rows + r0;
@@ -124,8 +133,9 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
                 const bool in = key < k_end;
                 const T *src =
                     (kv ? vbase : kbase) + static_cast<size_t>(in ? key : 0) * D + ch * 8;
-                uint8_t *dst = smem + (kv ? L::kVOff : L::kKOff) + stage * L::kTileBytes +
-                               row * L::kRowBytes + ch * 16;
+                uint8_t *dst = kv ? smem + L::kVOff + stage * L::kVTileBytes + row * L::kVRowBytes
+                                  : smem + L::kKOff + stage * L::kKTileBytes + row * L::kKRowBytes;
+                dst += ch * 16;
                 cp_async_16(dst, src, in);
             }
         }
@@ -155,21 +165,22 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         __syncthreads();  // ... everyone's part; and everyone is done with tile t - 1
         load_tile(t + kStages - 1);  // into the stage tile t - 1 used
 
-        {  // A: partial dots of key `lane` over columns [warp * D/4, (warp + 1) * D/4)
-            const uint8_t *krow =
-                smem + L::kKOff + stage * L::kTileBytes + lane * L::kRowBytes + warp * kQuarter * 2;
+        {  // A: partial dots of key `kl` over columns [c0, c0 + D/8), c0 = warp * D/4 + half * D/8
+            const uint8_t *krow = smem + L::kKOff + stage * L::kKTileBytes + kl * L::kKRowBytes +
+                                  (warp * kQuarter + half * kHalf) * 2;
             float2 dot[RPC];  // even and odd columns summed apart (paired fp32 FMAs)
 #pragma unroll
             for (int r = 0; r < RPC; ++r) dot[r] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c8 = 0; c8 < kQuarter / 8; ++c8) {
+            for (int c8 = 0; c8 < kHalf / 8; ++c8) {
                 const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8 * 16);
                 const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y),
                              k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
 #pragma unroll
                 for (int r = 0; r < RPC; ++r) {  // rows past nrows hold zeros
                     const float4 *qv =
-                        reinterpret_cast<const float4 *>(qs + r * D + warp * kQuarter + c8 * 8);
+                        reinterpret_cast<const float4 *>(qs + r * D + warp * kQuarter +
+                                                         half * kHalf + c8 * 8);
                     const float4 a = qv[0], c = qv[1];
                     float2 d = dot[r];
                     d = ffma2(make_float2(a.x, a.y), k0, d);
@@ -180,39 +191,42 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
                 }
             }
 #pragma unroll
-            for (int r = 0; r < RPC; ++r)
-                part[(warp * RPC + r) * kKeys + lane] = dot[r].x + dot[r].y;
+            for (int r = 0; r < RPC; ++r) {  // the two column halves of key kl summed
+                float sp = dot[r].x + dot[r].y;
+                sp += __shfl_xor_sync(0xffffffffu, sp, 16);
+                if (half == 0) part[(warp * RPC + r) * kKeys + kl] = sp;
+            }
         }
         __syncthreads();
         {  // A2: warp w owns rows w, w + 4, w + 8, w + 12
-            const int key = k_begin + kKeys * t + lane;
+            const int key = k_begin + kKeys * t + kl;
 #pragma unroll
             for (int i = 0; i < kRowsA2; ++i) {
                 const int r = warp + 4 * i;
                 if (r < nrows) {
                     const int gr = r0 + r;
                     const int last = p.causal ? len - p.Nq + gr % p.Nq : len - 1;
-                    float s = part[r * kKeys + lane] + part[(RPC + r) * kKeys + lane] +
-                              part[(2 * RPC + r) * kKeys + lane] +
-                              part[(3 * RPC + r) * kKeys + lane];
+                    float s = part[r * kKeys + kl] + part[(RPC + r) * kKeys + kl] +
+                              part[(2 * RPC + r) * kKeys + kl] +
+                              part[(3 * RPC + r) * kKeys + kl];
                     if (key >= k_end || key > last) s = -INFINITY;
-                    const float m_new = fmaxf(m_run[i], warp_max(s));
+                    const float m_new = fmaxf(m_run[i], half_max(s));
                     float alpha = 1.f, pr = 0.f;
                     if (m_new != -INFINITY) {  // ex2(-inf) = 0 covers masked keys, first tile
                         alpha = ex2(m_run[i] - m_new);
                         pr = ex2(s - m_new);
                     }
-                    l_run[i] = l_run[i] * alpha + warp_sum(pr);
+                    l_run[i] = l_run[i] * alpha + half_sum(pr);
                     m_run[i] = m_new;
-                    ps[r * kKeys + lane] = pr;
+                    if (half == 0) ps[r * kKeys + kl] = pr;
                     if (lane == 0) alpha_s[r] = alpha;
                 }
             }
         }
         __syncthreads();
         {  // B: O_g = alpha O_g + P V over this thread's key group, two columns, every row
-            const uint8_t *vcol = smem + L::kVOff + stage * L::kTileBytes +
-                                  rs * kKeysB * L::kRowBytes + cp * 4;
+            const uint8_t *vcol = smem + L::kVOff + stage * L::kVTileBytes +
+                                  rs * kKeysB * L::kVRowBytes + cp * 4;
             const float *pg = ps + rs * kKeysB;
 #pragma unroll
             for (int r = 0; r < RPC; ++r) {
@@ -227,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     vv[u] = unpack2<BF16>(
-                        *reinterpret_cast<const uint32_t *>(vcol + (k4 + u) * L::kRowBytes));
+                        *reinterpret_cast<const uint32_t *>(vcol + (k4 + u) * L::kVRowBytes));
 #pragma unroll
                 for (int r = 0; r < RPC; ++r) {
                     if (r < nrows) {  // rows past nrows have no probabilities this tile
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     }
     __syncthreads();  // every thread is past its last read of the K/V ring
     // merge of the key groups: group g's partial output of row r at red[(g * RPC + r) * D]
-    float *red = reinterpret_cast<float *>(smem + L::kKOff);
+    float *red = reinterpret_cast<float *>(smem);
 #pragma unroll
     for (int r = 0; r < RPC; ++r)
         if (r < nrows) reinterpret_cast<float2 *>(red + (rs * RPC + r) * D)[cp] = acc[r];

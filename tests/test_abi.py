@@ -122,10 +122,13 @@ def test_gqa_workspace_and_validation(lib):
 
 def test_decode_workspace_and_validation(lib):
     p = ctypes.c_void_p(16)
-    # 16 sequences x 8 K/V heads at 8k: 128 CTAs per key range; 14 ranges (of 608 keys) give
-    # about twelve CTAs per SM of a 152-SM GPU (1824 / 128 = 14)
+    # 16 sequences x 8 K/V heads at 8k: 128 CTAs per key range; about 28 CTAs per SM of a
+    # 152-SM GPU would take 4256 / 128 = 33 ranges, capped at 8192 / 256 = 32 (of 256 keys)
     rows = 16 * 32 * 1
-    assert api.decode_workspace_bytes(16, 32, 8, 1, 8192, 128) == 14 * rows * (128 + 2) * 4
+    assert api.decode_workspace_bytes(16, 32, 8, 1, 8192, 128) == 32 * rows * (128 + 2) * 4
+    # 2 sequences x 2 K/V heads at 64k: 4256 / 4 = 1064 ranges of 64 keys would be too short;
+    # 65536 / 256 = 256 ranges of 256 keys
+    assert api.decode_workspace_bytes(2, 8, 2, 1, 65536, 64) == 256 * 16 * (64 + 2) * 4
     # 256 keys or fewer: a single range, no scratch
     assert api.decode_workspace_bytes(2, 4, 4, 1, 200, 64) == 0
     assert lib.fa_decode_workspace_bytes(1, 6, 4, 1, 100, 64) == 0  # 4 does not divide 6
