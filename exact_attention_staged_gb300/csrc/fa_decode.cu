@@ -303,18 +303,21 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
 }
 
 // Merge of the key ranges of every row, in range order: M = max m_s, w_s = 2^(m_s - M),
-// l = sum w_s l_s, O = sum w_s O_s / l, LSE = (M + log2 l) ln 2.  One warp per row.
+// l = sum w_s l_s, O = sum w_s O_s / l, LSE = (M + log2 l) ln 2.  One CTA of four warps per
+// row: warp q sums the q-th quarter of the ranges in order, the four partial sums are added in
+// the order q = 0..3 (deterministic).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
     using T = elem_t<BF16>;
     constexpr int kCols = D / 32;
+    constexpr int kBatch = 8;  // ranges whose partial outputs are in flight at once
+    __shared__ float red_o[4][D];
+    __shared__ float red_l[4];
     const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
-    const long row = static_cast<long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= total_rows) return;
+    const long row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
-    // the ranges' statistics 32 at a time, lane s holding range s: M, the weights 2^(m_s - M)
-    // and l = sum w_s l_s by shuffles; then O = sum w_s O_s (the weights come from the lanes)
+    // every warp finds M over all ranges, 32 at a time, lane s holding range s
     float M = -INFINITY;
     for (int s0 = 0; s0 < p.splits; s0 += 32) {
         const int s = s0 + lane;
@@ -323,13 +326,15 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const int per = (p.splits + 3) / 4;
+    const int sb = min(p.splits, warp * per), se = min(p.splits, sb + per);
     float lsum = 0.f, acc[kCols];
 #pragma unroll
     for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
-    for (int s0 = 0; s0 < p.splits; s0 += 32) {
+    for (int s0 = sb; s0 < se; s0 += 32) {
         const int s = s0 + lane;
-        float w = 0.f, lw = 0.f;
-        if (s < p.splits) {
+        float w = 0.f, lw = 0.f;  // the weights come from the lanes
+        if (s < se) {
             const float2 st = ml[static_cast<long>(s) * total_rows + row];
             if (st.x != -INFINITY) {  // an empty range (also covers M = -inf) weighs nothing
                 w = ex2(st.x - M);
@@ -339,13 +344,13 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
         lsum += lw;
-        // eight ranges' partial outputs loaded before any is used, so their latencies overlap;
-        // a range past the last one reads as zero with weight zero (its lane's w is 0)
-        const int n = min(32, p.splits - s0);
-        for (int i0 = 0; i0 < n; i0 += 8) {
-            float x[8][kCols];
+        // a batch of ranges' partial outputs loaded before any is used, so their latencies
+        // overlap; a range past the warp's last one reads as zero with weight zero
+        const int n = min(32, se - s0);
+        for (int i0 = 0; i0 < n; i0 += kBatch) {
+            float x[kBatch][kCols];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kBatch; ++u) {
                 const int i = i0 + u;
                 const float *src = p.part_o +
                                    (static_cast<long>(s0 + min(i, n - 1)) * total_rows + row) * D +
@@ -354,19 +359,32 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
                 for (int c = 0; c < kCols; ++c) x[u][c] = i < n ? src[c] : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kBatch; ++u) {
                 const float wi = __shfl_sync(0xffffffffu, w, i0 + u);
 #pragma unroll
                 for (int c = 0; c < kCols; ++c) acc[c] = fmaf(wi, x[u][c], acc[c]);
             }
         }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    if (lane == 0) red_l[warp] = lsum;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) red_o[warp][lane * kCols + c] = acc[c];
+    __syncthreads();
+    if (warp != 0) return;
+    const float l = red_l[0] + red_l[1] + red_l[2] + red_l[3];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     T *dst = reinterpret_cast<T *>(p.o) + row * D + lane * kCols;
 #pragma unroll
-    for (int c = 0; c < kCols; c += 2)
-        reinterpret_cast<uint32_t *>(dst + c)[0] = pack2<BF16>(acc[c] * inv, acc[c + 1] * inv);
-    if (lane == 0) p.lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+    for (int c = 0; c < kCols; c += 2) {
+        float o2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int col = lane * kCols + c + e;
+            o2[e] = red_o[0][col] + red_o[1][col] + red_o[2][col] + red_o[3][col];
+        }
+        reinterpret_cast<uint32_t *>(dst + c)[0] = pack2<BF16>(o2[0] * inv, o2[1] * inv);
+    }
+    if (lane == 0) p.lse[row] = l > 0.f ? (M + __log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
 template <int D, bool BF16, int RPC>
@@ -392,8 +410,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     else e = launch_decode_rpc<D, BF16, 16>(p, stream);
     if (e != cudaSuccess || p.splits == 1) return e;
     const long rows = static_cast<long>(p.B) * p.H * p.Nq;
-    fa_decode_combine_kernel<D, BF16>
-        <<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+    fa_decode_combine_kernel<D, BF16><<<static_cast<unsigned>(rows), 128, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
