@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
 FA_FP16, FA_BF16 = 0, 1
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, -1, -2, -3, -4
+FA_ERR_INTERNAL = -5
 FA_NOALLOC_MAX_ROWS = 1 << 20  # B*H*N limit of fa_bwd_noalloc
 
 # exported names and their signatures, in the order include/fa.h declares them

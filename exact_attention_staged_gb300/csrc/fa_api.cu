@@ -533,6 +533,8 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    int dtype, float scale, int causal, const uint8_t *block_mask, void *stream) {
     int rc = check_shape(B, H, N, d, dtype, scale);
     if (rc != FA_OK) return rc;
+    rc = check_mask(block_mask, N);
+    if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv});
     if (rc != FA_OK) return rc;
     if (static_cast<size_t>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID;
@@ -670,6 +672,7 @@ const char *fa_status_string(int code) {
         case FA_ERR_UNSUPPORTED: return "unsupported head dimension or device";
         case FA_ERR_CUDA: return "CUDA runtime error";
         case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case FA_ERR_INTERNAL: return "kernel found its shared memory misaligned";
         default: return "unknown status";
     }
 }

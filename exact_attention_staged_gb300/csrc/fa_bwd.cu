@@ -19,9 +19,9 @@
 //   dQ           CTA = one 128-row query tile i.  For every live key tile j:
 //                  S = Q_i K_j^T, dP = dO_i V_j^T, P = exp2(...), dS = P o (dP - D_i),
 //                  dQ += dS K_j (TS MMA), and finally dQ *= scale.
-// In both, two groups of four warps split every 128 x 128 score tile into two 64-wide column
-// halves, and the MMA warp runs one tile ahead so the groups' exponentials overlap the tensor
-// core (see each kernel's comment for its order).
+// In both, four groups of four warps split every 128 x 128 score tile into four 32-wide column
+// quarters (one TMEM lane quadrant per warp of a group), and the MMA warps run one tile ahead so
+// the groups' exponentials overlap the tensor core (see each kernel's comment for its order).
 #include "fa_internal.h"
 
 #include <cmath>
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dV, dK
     extern __shared__ uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // layouts assume a 1024-aligned base; never observed
-        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrTimeout);
+        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrInternal);
         return;
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     constexpr uint32_t kIdescTS = idesc_f16(128, D, BF16, true);     // dQ
     extern __shared__ uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // layouts assume a 1024-aligned base; never observed
-        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrTimeout);
+        if (threadIdx.x == 0) atomicExch(p.ctl.status, kErrInternal);
         return;
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);

@@ -28,6 +28,7 @@ struct Ctl {
 };
 
 constexpr int kErrTimeout = -4;
+constexpr int kErrInternal = -5;  // shared memory misplaced: the kernel did not run
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -54,7 +54,10 @@ enum {
     FA_ERR_INVALID = -1,      /* null or misaligned pointer, bad size, bad scale */
     FA_ERR_UNSUPPORTED = -2,  /* head dimension other than 64/128, or no sm_103 device */
     FA_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, attribute, symbol) */
-    FA_ERR_TIMEOUT = -4       /* a device pipeline wait ran out of time (from fa_sync_status) */
+    FA_ERR_TIMEOUT = -4,      /* a device pipeline wait ran out of time (from fa_sync_status) */
+    FA_ERR_INTERNAL = -5      /* a kernel found its shared memory misplaced (its base not
+                                 1024-byte aligned) and returned without computing; never
+                                 expected (from fa_sync_status) */
 };
 
 /*
@@ -200,7 +203,8 @@ int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, con
  *
  * The D scratch lives in a fixed array compiled into libfa.so: FA_NOALLOC_MAX_ROWS floats
  * (4 MiB) that every GPU which loads the library keeps until the process exits.
- *  - Returns FA_ERR_INVALID, launching nothing, when B * H * N > FA_NOALLOC_MAX_ROWS.
+ *  - Returns FA_ERR_INVALID, launching nothing, when B * H * N > FA_NOALLOC_MAX_ROWS, or
+ *    when the block mask is wider than fa_bwd allows.
  *  - The first call on a device looks up the array's device address with that device current;
  *    make that first call before any stream capture.
  *  - Every call on a device uses the same array, which keeps the last call's values.  Calls
@@ -239,7 +243,8 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
 /*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a pipeline wait and returned early; its outputs
- * are undefined) or FA_ERR_CUDA (the stream reported an error).
+ * are undefined), FA_ERR_INTERNAL (a kernel refused to run on a misaligned shared-memory base;
+ * its outputs are undefined) or FA_ERR_CUDA (the stream reported an error).
  */
 int fa_sync_status(void *stream);
 

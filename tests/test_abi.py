@@ -33,6 +33,23 @@ def test_header_declares_the_boundary():
     assert len(names) == len(set(names))
 
 
+def header_constants():
+    """Every FA_* integer the header defines: enum members and #define'd values."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {m.group(1): int(m.group(2)) for m in
+           re.finditer(r"\b(FA_[A-Z_0-9]+)\s*=\s*(-?\d+)", text)}
+    for m in re.finditer(r"#define\s+(FA_[A-Z_0-9]+)\s+\(1u\s*<<\s*(\d+)\)", text):
+        out[m.group(1)] = 1 << int(m.group(2))
+    return out
+
+
+def test_binding_constants_match_the_header():
+    consts = header_constants()
+    for name in ("FA_FP16", "FA_BF16", "FA_OK", "FA_ERR_INVALID", "FA_ERR_UNSUPPORTED",
+                 "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_INTERNAL", "FA_NOALLOC_MAX_ROWS"):
+        assert getattr(api, name) == consts[name], name
+
+
 def test_library_exports_every_declared_symbol(lib):
     names = header_functions()
     for n in names:
@@ -44,6 +61,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_workspace_size(lib):
     assert api.status_string(0) == "ok"
     assert "timed out" in api.status_string(api.FA_ERR_TIMEOUT)
+    assert "misaligned" in api.status_string(api.FA_ERR_INTERNAL)
     assert api.status_string(12345) == "unknown status"
     assert api.workspace_bytes(1, 1, 1, 64) == 256
     assert api.workspace_bytes(2, 16, 4096, 128) == 2 * 16 * 4096 * 4

@@ -121,3 +121,18 @@ def test_stored_traffic_is_used_only_while_the_kernel_sources_match(monkeypatch)
     monkeypatch.setitem(bench.KERNEL_SOURCES, "fa_decode_kernel", ("bench.py",))
     assert bench.ncu_traffic("fa_decode_kernel", "decode_gqa_d128_kv8k") is None
     assert bench.decode_traffic("decode_gqa_d128_kv8k", 1) is None
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_regions():
+    clk = bench.ClockSampler(0)
+    line = "{},2070,Not Active,Not Active,Not Active,{}"
+    clk.samples = [(0.5, line.format(1500, "Not Active")),   # before the first region
+                   (1.2, line.format(2070, "Not Active")),
+                   (1.8, line.format(2000, "Active")),
+                   (2.5, line.format(900, "Active")),        # between regions
+                   (3.1, line.format(1980, "Not Active"))]
+    clk.windows = [(1.0, 2.0), (3.0, 3.5)]
+    s = clk.summary()
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 2000 and s["sm_mhz_min"] == 1980 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]

@@ -115,3 +115,24 @@ def test_gqa_workload_parity(cuda_lib):
     assert torch.isfinite(o).all()
     for x in grads:
         assert torch.isfinite(x).all()
+
+
+def test_gqa_split_groups_with_partial_last_head_group(cuda_lib):
+    # dK/dV with each K/V head's query group split over 2 CTAs per key tile: its CTA order then
+    # has B * H_kv * 2 = 24 work-unit heads, taken in groups of 16 at N = 4096, d = 128 (the
+    # streamed Q and dO tiles of a group stay near 32 MiB of L2), so the last group is partial
+    from test_parity_gpu import heads_per_group
+    B, H, Hkv, N, d = 2, 12, 6, 4096, 128
+    units = B * Hkv * 2
+    grp = heads_per_group(units, N, d, 2.0)
+    assert units > grp and units % grp != 0
+    t = make_inputs(B, H, N, d, torch.bfloat16, seed=440, h_kv=Hkv)
+    scale = 1 / math.sqrt(d)
+    cuda_lib.debug_set_dkdv_splits(2)
+    try:
+        o, lse, grads = run_gqa(cuda_lib, t, scale, True)
+    finally:
+        cuda_lib.debug_set_dkdv_splits(0)
+    ref = oracle.attention_gqa(t["q"], t["k"], t["v"], scale, True, dout=t["do"])
+    check_fwd(o, lse, ref, "gqa split, partial group")
+    check_bwd(grads, ref, "gqa split, partial group")

@@ -503,6 +503,29 @@ def test_fp8_attention_is_attention_of_the_decoded_values():
         assert not np.isnan(oracle.e4m3_to_f64(t[x])).any()
 
 
+def test_fp8_descales_in_a_two_key_closed_form():
+    # one query against two keys is a logistic choice between the two value rows; written out
+    # by hand from the codes: q = 1.0 (0x38), k0 = 2.0 (0x40), k1 = 0.5 (0x30), v0 = 1.5 (0x3C),
+    # v1 = -1.0 (0xB8), so s_i = scale * dq * dk * q k_i and O = dv (1.5 s(s0 - s1) - s(s1 - s0))
+    # with s the logistic function; the descales of Q and K enter only through the scores, the
+    # descale of V only as a factor of O
+    q = np.array([[[[0x38]]]], dtype=np.uint8)
+    k = np.array([[[[0x40], [0x30]]]], dtype=np.uint8)
+    v = np.array([[[[0x3C], [0xB8]]]], dtype=np.uint8)
+    for scale, dq, dk, dv in ((0.5, 1.0, 1.0, 1.0), (0.7, 0.25, 3.0, 2.5), (1.3, 2.0, 0.125, 0.1)):
+        s0, s1 = scale * dq * dk * 2.0, scale * dq * dk * 0.5
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        want_o = dv * (1.5 * w0 - 1.0 * (1.0 - w0))
+        want_lse = math.log(math.exp(s0) + math.exp(s1))
+        # two query rows: row 0 sees only key 0 under the causal mask, row 1 sees both
+        qq = np.concatenate([q, q], axis=2)
+        got = oracle.attention_fp8(qq, k, v, scale, dq, dk, dv, causal=True)
+        np.testing.assert_allclose(got["o"][0, 0, 1, 0], want_o, rtol=1e-14, atol=1e-15)
+        np.testing.assert_allclose(got["lse"][0, 0, 1], want_lse, rtol=1e-14)
+        np.testing.assert_allclose(got["o"][0, 0, 0, 0], dv * 1.5, rtol=1e-15)
+        np.testing.assert_allclose(got["lse"][0, 0, 0], s0, rtol=1e-14)
+
+
 # ---------------------------------------------------------------- dropout
 from oracle import dropout as odrop  # noqa: E402
 

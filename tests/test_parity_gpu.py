@@ -258,8 +258,38 @@ def test_invalid_arguments_on_device(cuda_lib):
 
 # ---------------------------------------------------------------- the five workloads
 
-def _sampled_heads(BH):
-    return sorted({0, BH - 1})
+def _spread(total, pick):
+    """`pick` indices spread evenly over range(total), first and last included."""
+    if total <= pick:
+        return list(range(total))
+    return sorted({round(i * (total - 1) / (pick - 1)) for i in range(pick)})
+
+
+def sample_rows(N, seed, edge=16, mid=32):
+    """The first and last `edge` rows of a head and `mid` seeded random rows in between."""
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(edge, N))) | set(range(max(0, N - edge), N))
+    rows |= set(rng.choice(N, size=min(mid, N), replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_fwd_rows(o, lse, rows, ref_o, ref_lse, what):
+    """Sampled rows of one head against oracle.forward_rows, with the forward's tolerances."""
+    got_o, got_l = np64(o)[rows], np64(lse)[rows]
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(got_l), ~fin), f"{what}: -inf LSE rows differ"
+    err = float(np.max(np.abs(got_o - ref_o)))
+    rel = relf(got_o, ref_o)
+    lerr = float(np.max(np.abs(got_l[fin] - ref_lse[fin]))) if fin.any() else 0.0
+    assert err <= O_MAX and rel <= O_REL, f"{what}: O maxabs {err:.3e} relF {rel:.3e}"
+    assert lerr <= LSE_MAX, f"{what}: LSE maxabs {lerr:.3e}"
+
+
+# heads compared in full (forward and backward) per workload: every head where the oracle is
+# quick, otherwise heads spread over the whole B*H range, so that every group of heads in the
+# kernels' CTA order (heads are scheduled in groups that share L2) has a head checked in full
+FULL_HEADS = {"tiny_fwd_fp16": 1, "dense_d64_n1k": 64, "causal_d128_n4k": 32,
+              "gpt_causal_d128_n8k": 8, "blocksparse_d64_n16k": 3}
 
 
 @pytest.mark.parametrize("name", ["tiny_fwd_fp16", "dense_d64_n1k", "causal_d128_n4k",
@@ -271,14 +301,47 @@ def test_workload_parity(cuda_lib, name):
     o, lse, grads = run_pair(cuda_lib, t, w.scale, w.causal, mask, backward=w.backward)
     BH = w.B * w.H
     flat = {x: t[x].reshape(BH, w.N, w.d) for x in ("q", "k", "v", "do")}
-    for h in _sampled_heads(BH):
+    of, lf = o.reshape(BH, w.N, w.d), lse.reshape(BH, w.N)
+    # every head: 64 sampled rows of O and LSE, each row computed alone by the oracle
+    for h in range(BH):
+        rows = sample_rows(w.N, 1000 * w.seed + h)
+        ro, rl = oracle.forward_rows(flat["q"][h], flat["k"][h], flat["v"][h], w.scale, rows,
+                                     w.causal, mask)
+        check_fwd_rows(of[h], lf[h], rows, ro, rl, f"{name} head {h} sampled rows")
+    # heads spread over the CTA order: the whole head, forward and backward
+    for h in _spread(BH, FULL_HEADS[name]):
         ref = oracle.attention(flat["q"][h], flat["k"][h], flat["v"][h], w.scale, w.causal,
                                mask, dout=flat["do"][h] if w.backward else None)
-        check_fwd(o.reshape(BH, w.N, w.d)[h], lse.reshape(BH, w.N)[h], ref, f"{name} head {h}")
+        check_fwd(of[h], lf[h], ref, f"{name} head {h}")
         if w.backward:
             check_bwd([g.reshape(BH, w.N, w.d)[h] for g in grads], ref, f"{name} head {h}")
-    # every head is finite and LSE never exceeds what its scores allow
     assert torch.isfinite(o).all()
     if w.backward:
         for g in grads:
             assert torch.isfinite(g).all()
+
+
+def heads_per_group(units, N, d, tensors_per_unit):
+    """The host's CTA-order group size: as many work-unit heads as keep about 32 MiB of
+    streamed 16-bit [N, d] tensors in flight (at least 1, at most `units`)."""
+    g = int((32.0 * 1024 * 1024) // (2.0 * N * d * tensors_per_unit))
+    return max(1, min(g, units))
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(3, 4, 8192, 128, True), (5, 8, 4096, 64, False)])
+def test_partial_last_head_group(cuda_lib, B, H, N, d, causal):
+    # B*H is larger than the CTA-order group and not a multiple of it (8192 x 128: groups of 8
+    # heads for 12 heads; 4096 x 64: groups of 32 for 40), so the last group is partial in the
+    # forward, dK/dV and dQ grids; every head is compared in full with the oracle
+    BH = B * H
+    grp = heads_per_group(BH, N, d, 2.0)
+    assert BH > grp and BH % grp != 0
+    t = make_inputs(B, H, N, d, torch.bfloat16, seed=70 + d)
+    scale = 1 / math.sqrt(d)
+    o, lse, grads = run_pair(cuda_lib, t, scale, causal)
+    flat = {x: t[x].reshape(BH, N, d) for x in ("q", "k", "v", "do")}
+    for h in range(BH):
+        ref = oracle.attention(flat["q"][h], flat["k"][h], flat["v"][h], scale, causal,
+                               dout=flat["do"][h])
+        check_fwd(o.reshape(BH, N, d)[h], lse.reshape(BH, N)[h], ref, f"head {h}")
+        check_bwd([g.reshape(BH, N, d)[h] for g in grads], ref, f"head {h}")

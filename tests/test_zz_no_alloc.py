@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_attention_staged_gb300.workloads import make_block_mask, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -54,12 +55,22 @@ def test_noalloc_backward_matches_workspace_backward_twice(cuda_lib):
         o, lse = cuda_lib.fwd(q, k, v, scale, causal=causal, block_mask=mask)
         ref = cuda_lib.bwd(q, k, v, o, lse, do, scale, causal=causal, block_mask=mask)
         dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         rc = _noalloc(lib, q, k, v, o, lse, do, dq, dk, dv, scale, causal, mask)
         assert rc == cuda_lib.FA_OK, cuda_lib.status_string(rc)
         assert cuda_lib.sync_status() == 0
+        # no device memory was taken by the call (cudaMalloc works in pages of at least 2 MiB)
+        assert torch.cuda.mem_get_info()[0] == free_before
         for got, want in zip((dq, dk, dv), ref):
             assert torch.isfinite(got).all()
             assert _relf(got, want) <= G_REL
+        # and against the fp64 oracle itself, not only the workspace backward
+        want = oracle.attention(t["q"], t["k"], t["v"], scale, causal,
+                                None if mask is None else mask.cpu(), dout=t["do"])
+        for name, got in zip(("dq", "dk", "dv"), (dq, dk, dv)):
+            r = _relf(got, torch.from_numpy(want[name]))
+            assert r <= G_REL, f"{name} relF {r:.3e} against the oracle"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
