@@ -577,7 +577,8 @@ int fa_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse,
     fa::Fp8Maps maps;
     if (make_map_bytes(&maps.q, q, d, N, static_cast<long>(B) * H, d, fa::kTile) ||
         make_map_bytes(&maps.k, k, d, N, static_cast<long>(B) * H_kv, d, fa::kTile) ||
-        make_map_bytes(&maps.vt, vt, Np, d, static_cast<long>(B) * H_kv, fa::kTile, d))
+        make_map_bytes(&maps.vt, vt, Np, d, static_cast<long>(B) * H_kv, fa::kTile, d) ||
+        make_map(&maps.o, o, B * H, N, d, FA_BF16))
         return FA_ERR_CUDA;
     fa::Fp8FwdParams p;
     p.o = o;

@@ -18,7 +18,9 @@
 // CTA and TMEM layout as fa_fwd.cu: two query tiles (256 rows), 384 threads (TMA warp, MMA
 // warp, two idle warps whose registers go to the softmax warpgroups, 2 x 4 softmax warps), S_t
 // at columns [128 t, 128 t + 128), O_t at 256 + t d; P~_t packed four per column over the
-// first 32 columns of S_t.
+// first 32 columns of S_t.  O_t (bf16, twice the size of the e4m3 Q_t tile) is staged in the
+// box layout of its tensor map over K/V ring slots 2t and 2t + 1, idle once every MMA of the CTA
+// has completed, and written by TMA.
 #include "fa_internal.h"
 
 #include <cmath>
@@ -56,7 +58,8 @@ template <int D>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmvt, const Fp8FwdParams p) {
+                      const __grid_constant__ CUtensorMap tmvt,
+                      const __grid_constant__ CUtensorMap tmo, const Fp8FwdParams p) {
     using L = Fp8Layout<D>;
     constexpr uint32_t kIdescS = idesc_e4m3(128, 128);
     constexpr uint32_t kIdescPV = idesc_e4m3(128, D);
@@ -255,9 +258,11 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     if (ok) umma_commit_el(&empty[prev_vs]);
                 }
+                // both tiles' o_final complete once every MMA issued above has: the ring is then
+                // idle, and each softmax group stages its O over two of its slots
                 if (ok) {
-                    for (int t = 0; t < 2; ++t)
-                        if (cnt[t] > 0) umma_commit_el(&o_final[t]);
+                    umma_commit_el(&o_final[0]);
+                    umma_commit_el(&o_final[1]);
                 }
                 umma_commit_el(drain);
                 drain_wait(drain, 0, p.ctl);
@@ -347,15 +352,17 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive_warp_after_st(&p_full[t]);
             ++cnt;
         }
-        if (ok && cnt > 0) {
+        if (ok) {
             ok = mbar_wait_warp(&o_final[t], 0, p.ctl, abort_flag);
             tc_fence_after();
         }
+        // O_t = O~_t * descale_v / l staged as bf16 boxes over ring slots 2t, 2t + 1 and written
+        // by TMA.  All four warps of the group reach the named barrier, whether or not their
+        // waits succeeded.
+        constexpr int kBoxBytes = kTile * 128;
+        uint8_t *stage = smem + L::kSlotOff + t * 2 * L::kTileBytes;
         if (ok) {
             const float inv = l > 0.f ? p.descale_v / l : 0.f;
-            const bool valid = q_row < p.N;
-            __nv_bfloat16 *orow =
-                reinterpret_cast<__nv_bfloat16 *>(p.o) + (static_cast<size_t>(bh) * p.N + q_row) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
@@ -366,22 +373,19 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack2<true>(__uint_as_float(o[2 * e]) * inv,
-                                       __uint_as_float(o[2 * e + 1]) * inv);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-                }
+                st_box_row<true, 32>(stage + (cc >> 1) * kBoxBytes, row, (cc & 1) * 32, o, inv);
             }
-            if (valid)
+            fence_proxy_async_smem();
+            if (q_row < p.N)
                 p.lse[static_cast<size_t>(bh) * p.N + q_row] =
                     l > 0.f ? (m - kOff + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+        named_sync(1 + t, 128);
+        if (quad == 0 && lane == 0 && ok && *abort_flag == 0 && qt * kTile < p.N) {
+            for (int b = 0; b < D / 64; ++b)
+                tma_store_3d(&tmo, stage + b * kBoxBytes, b * 64, qt * kTile, bh);
+            bulk_commit();
+            bulk_wait_read_all();
         }
     }
 
@@ -438,7 +442,7 @@ cudaError_t launch_fwd_fp8_t(const Fp8Maps &maps, const Fp8FwdParams &p, cudaStr
     if (e != cudaSuccess) return e;
     const long grid = static_cast<long>(p.BH) * p.num_pairs;
     kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(maps.q, maps.k,
-                                                                           maps.vt, p);
+                                                                           maps.vt, maps.o, p);
     return cudaGetLastError();
 }
 

@@ -123,6 +123,7 @@ struct Fp8FwdParams {
 struct Fp8Maps {
     CUtensorMap q, k;         // [B*H or B*H_kv, N, d] bytes, boxes d x 128 rows
     CUtensorMap vt;           // [B*H_kv, d, Np] bytes (V transposed), boxes 128 keys x d rows
+    CUtensorMap o;            // [B*H, N, d] bf16 output, boxes 64 elements x 128 rows
 };
 
 // Decode: a few new query rows per sequence against a KV cache (see fa_decode.cu).
