@@ -1,10 +1,13 @@
 """Benchmark: exact-attention forward + backward through the C ABI on GB300.
 
-One step = one pass of the whole hot path over one batch: fa_fwd (forward kernel), then the
-backward's three stages (D pre-pass, dK/dV kernel, dQ kernel), on the GPT-style long-context
-training shape (causal, B=1 H=32 N=8192 d=128, bf16, Q and K doubled).  Inputs are resident in
-HBM before timing; the step's working set (Q, K, V, dO, O, dQ, dK, dV: 537 MB) is larger than
-the 129 MB L2, so no flush is done between steps.
+One step = one pass of the whole hot path over one batch: fa_fwd (forward kernel), then fa_bwd
+(the D pre-pass, then the dQ and dK/dV kernels, whose grids overlap inside the call), on the
+GPT-style long-context training shape (causal, B=1 H=32 N=8192 d=128, bf16, Q and K doubled).
+Inputs are resident in HBM before timing; the step's working set (Q, K, V, dO, O, dQ, dK, dV:
+537 MB) is larger than the 129 MB L2, so no flush is done between steps.  The K-step timed
+region is repeated back to back until half a second of work is timed (--min-region-s), so the
+clock record holds tens of samples.  Per-kernel durations (the roofline's dominant kernel) come
+from a separate pass of K steps with the backward's kernels launched one by one.
 
 FLOP convention (FlashAttention-2 reading notes, reproducibility section): forward 4*N^2*d per
 head, backward 2.5x that, both halved for causal attention.
@@ -397,17 +400,18 @@ def run_gpu(args, w):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.current_stream()
     gqa = w.h_kv is not None or w.dropout > 0
+    # one step: the forward kernel, then the whole backward call (D, dQ and dK/dV, whose grids
+    # overlap inside the call), each timed as one unit
+    names = ["fa_fwd_kernel", "fa_bwd_gqa" if w.dropout == 0 else "fa_bwd_dropout"] if gqa \
+        else ["fa_fwd_kernel", "fa_bwd"]
     if gqa:
-        # grouped K/V heads or dropout: the forward kernel, then the whole backward call (D,
-        # dK/dV, dQ), timed as one unit
-        names = ["fa_fwd_kernel", "fa_bwd_gqa" if w.dropout == 0 else "fa_bwd_dropout"]
         workspace = torch.empty(api.gqa_workspace_bytes(w.B, w.H, w.kv_heads, w.N, w.d),
                                 dtype=torch.uint8, device=dev)
         delta = workspace
     else:
-        names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel",
-                 "fa_bwd_dq_kernel"]
         delta = torch.empty_like(lse)
+    stage_names = ["fa_fwd_kernel", "fa_bwd_preprocess_kernel", "fa_bwd_dkdv_kernel",
+                   "fa_bwd_dq_kernel"]
 
     def fwd_call():
         if w.dropout > 0:
@@ -436,16 +440,20 @@ def run_gpu(args, w):
         mark(0)
         fwd_call()
         mark(1)
-        if gqa:
-            bwd_call()
-            mark(2)
-            return
-        api.bwd_preprocess(o, do, delta)
+        bwd_call()
         mark(2)
+
+    def stage_step(events):
+        # the backward's three kernels called one by one (no overlap), for per-kernel times
+        events[0].record(stream)
+        fwd_call()
+        events[1].record(stream)
+        api.bwd_preprocess(o, do, delta)
+        events[2].record(stream)
         api.bwd_dkdv(q, k, v, do, lse, delta, dk, dv, w.scale, w.causal, mask)
-        mark(3)
+        events[3].record(stream)
         api.bwd_dq(q, k, v, do, lse, delta, dq, w.scale, w.causal, mask)
-        mark(4)
+        events[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -460,23 +468,46 @@ def run_gpu(args, w):
         raise RuntimeError("device status reported an error in the timed region")
     nsteps = len(ev)
     max_ms = sum(regions)
-    f = flops(w.B, w.H, w.N, w.d, w.causal, density)
-    if gqa:
-        f = {"fa_fwd_kernel": f["fa_fwd_kernel"],
-             names[1]: sum(f.values()) - f["fa_fwd_kernel"]}
+    f_stage = flops(w.B, w.H, w.N, w.d, w.causal, density)
+    f = {"fa_fwd_kernel": f_stage["fa_fwd_kernel"],
+         names[1]: sum(f_stage.values()) - f_stage["fa_fwd_kernel"]}
     step_flops = sum(f.values())
     value = world * step_flops * nsteps / (max_ms / 1e3) / 1e12
-    per_kernel = {}
-    for i, n in enumerate(names):
-        ms = [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(nsteps)]
-        per_kernel[n] = {"ms": statistics.mean(ms), "ms_median": statistics.median(ms),
-                         "ms_min": min(ms),
-                         "tflops": f[n] / (statistics.mean(ms) / 1e3) / 1e12}
+
+    def kernel_stats(evs, labels, fl):
+        out = {}
+        for i, n in enumerate(labels):
+            ms = [e[i].elapsed_time(e[i + 1]) for e in evs]
+            out[n] = {"ms": statistics.mean(ms), "ms_median": statistics.median(ms),
+                      "ms_min": min(ms), "tflops": fl[n] / (statistics.mean(ms) / 1e3) / 1e12}
+        return out
+
+    per_kernel = kernel_stats(ev, names, f)
     fwd_ms = per_kernel["fa_fwd_kernel"]["ms"]
-    bwd_ms = sum(per_kernel[n]["ms"] for n in names[1:])
+    bwd_ms = per_kernel[names[1]]["ms"]
     peaks = measured_peaks()
-    dominant = max(names, key=lambda n: per_kernel[n]["ms"])
-    achieved = per_kernel[dominant]["tflops"]
+    stages = None
+    if not gqa:
+        # per-kernel durations: K steps with the backward's kernels launched one by one and an
+        # event between each, after the timed regions (inside fa_bwd the dQ and dK/dV grids
+        # overlap, so their own durations are taken here)
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+               for _ in range(args.steps)]
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        for s_ in range(args.steps):
+            stage_step(sev[s_])
+        torch.cuda.synchronize()
+        if api.sync_status() != 0:
+            raise RuntimeError("device status reported an error in the per-kernel pass")
+        stages = kernel_stats(sev, stage_names, f_stage)
+        dominant = max(stage_names, key=lambda n: stages[n]["ms"])
+        achieved = stages[dominant]["tflops"]
+        timing = "per-kernel pass: the backward's kernels launched one by one, CUDA events"
+    else:
+        dominant = max(names, key=lambda n: per_kernel[n]["ms"])
+        achieved = per_kernel[dominant]["tflops"]
+        timing = "timed regions (the whole backward call as one unit)"
     # the timed regions last well under a second of back-to-back kernels: the burst peak is
     # the denominator; the fraction of the seconds-long sustained peak is given beside it
     peak = peaks["bf16_tflops"]
@@ -484,7 +515,8 @@ def run_gpu(args, w):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": ncu_traffic(dominant, w.name),
                 "peak_kind": f"bf16 dense burst ({peaks['source']})",
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "timing": timing}
 
     # ---- end to end through the C ABI from pinned host buffers
     # Two device buffer sets: step s copies its inputs from pinned host memory into set s % 2
@@ -607,6 +639,7 @@ def run_gpu(args, w):
                 "ms": bwd_ms},
         "frac_of_peak": value / world / peak,
         "kernels": per_kernel,
+        "kernel_stages": stages,
         "roofline": roofline,
         "mufu": mufu_bound(w, mask_cpu, fwd_ms, clk.summary()),
         "cpu_baseline": cpu,
@@ -672,21 +705,20 @@ def run_decode_gpu(args, w):
     torch.cuda.synchronize()
     if api.sync_status() != 0:
         raise RuntimeError("device status reported an error during warm-up")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    dist_barrier(world)
-    torch.cuda.synchronize()
+
+    def marked_step(events):
+        events[0].record(stream)
+        step()
+        events[1].record(stream)
+
     with ClockSampler(local) as clk:
-        ev[0].record(stream)
-        for s_ in range(args.steps):
-            step()
-            ev[s_ + 1].record(stream)
-        torch.cuda.synchronize()
-    dist_barrier(world)
-    elapsed_ms = ev[0].elapsed_time(ev[-1])
-    max_ms = dist_max(elapsed_ms, world, dev)
+        regions, ev = timed_regions(marked_step, args.steps, world, dev, stream,
+                                    args.min_region_s, 2, clk)
+    nsteps = len(ev)
+    max_ms = sum(regions)
     fl, nbytes = decode_work(w, t)
-    value = world * fl * args.steps / (max_ms / 1e3) / 1e12
-    step_ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
+    value = world * fl * nsteps / (max_ms / 1e3) / 1e12
+    step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     peaks = measured_peaks()
     gbs = nbytes / (step_ms / 1e3) / 1e9
     launches = 1 if nws == 0 else 2
@@ -737,7 +769,9 @@ def run_decode_gpu(args, w):
                "sample": f"the whole step ({w.B * w.H * w.Nq} rows), fp64 numpy, {secs:.1f} s"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / nsteps,
+        "timed_regions": {"steps_each": args.steps, "repeats": len(regions),
+                          "total_s": max_ms / 1e3},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "H_kv": w.h_kv, "Nq": w.Nq,
@@ -749,7 +783,7 @@ def run_decode_gpu(args, w):
         "cpu_baseline": cpu,
         "e2e": {"value": world * fl * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * nsteps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -782,24 +816,24 @@ def run_fp8_gpu(args, w):
     torch.cuda.synchronize()
     if api.sync_status() != 0:
         raise RuntimeError("device status reported an error during warm-up")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    dist_barrier(world)
-    torch.cuda.synchronize()
+
+    def marked_step(events):
+        events[0].record(stream)
+        step()
+        events[1].record(stream)
+
     with ClockSampler(local) as clk:
-        ev[0].record(stream)
-        for s_ in range(args.steps):
-            step()
-            ev[s_ + 1].record(stream)
-        torch.cuda.synchronize()
-    dist_barrier(world)
-    max_ms = dist_max(ev[0].elapsed_time(ev[-1]), world, dev)
+        regions, ev = timed_regions(marked_step, args.steps, world, dev, stream,
+                                    args.min_region_s, 2, clk)
+    nsteps = len(ev)
+    max_ms = sum(regions)
     if api.sync_status() != 0:
         raise RuntimeError("device status reported an error in the timed region")
     fl = flops(w.B, w.H, w.N, w.d, w.causal)["fa_fwd_kernel"]
-    value = world * fl * args.steps / (max_ms / 1e3) / 1e12
+    value = world * fl * nsteps / (max_ms / 1e3) / 1e12
     peaks = measured_peaks()
     peak = 2.0 * peaks["bf16_tflops"]  # e4m3 dense = 2 x bf16 dense (nominal 4.5 / 2.25 PF)
-    step_ms = max_ms / args.steps
+    step_ms = max_ms / nsteps
     hq, hk, hv = (t[x].pin_memory() for x in ("q", "k", "v"))
     ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -828,6 +862,8 @@ def run_fp8_gpu(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "timed_regions": {"steps_each": args.steps, "repeats": len(regions),
+                          "total_s": max_ms / 1e3},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
@@ -842,7 +878,7 @@ def run_fp8_gpu(args, w):
         "e2e": {"value": world * fl * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(x.numel() for x in (hq, hk, hv)),
                 "d2h_bytes_per_step": ho.numel() * 2 + hlse.numel() * 4, "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * nsteps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

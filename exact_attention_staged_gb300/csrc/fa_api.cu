@@ -61,9 +61,9 @@ int device_setup(int *dev_out, int **status_out) {
 // Snapshot of the debug hooks for one launch; the visit log must cover every tile of it.
 int make_ctl(int *status, int BH, int T, fa::Ctl *out) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_visit_log != nullptr &&
-        g_visit_bytes < static_cast<size_t>(BH) * static_cast<size_t>(T) * static_cast<size_t>(T))
-        return FA_ERR_INVALID;
+    // the marks are 32-bit atomic ORs: the log covers every tile, rounded up to whole words
+    const size_t need = static_cast<size_t>(BH) * static_cast<size_t>(T) * static_cast<size_t>(T);
+    if (g_visit_log != nullptr && g_visit_bytes < (need + 3) / 4 * 4) return FA_ERR_INVALID;
     fa::Ctl &c = *out;
     c.status = status;
     c.wait_limit_ns = g_wait_ns;
@@ -281,10 +281,11 @@ int bwd_params(const void *q, const void *k, const void *v, const void *dout, co
 
 // dK/dV (+ the group reduce when the K/V groups are split, sp.splits > 1); part: room for
 // part_bytes(sp, ...) of fp32 partial sums, or nullptr with one split.
+// after_dq: queued right after the dQ pass of the same call (see fa::launch_bwd_dkdv).
 int run_dkdv(const void *q, const void *k, const void *v, const void *dout, const float *lse,
              const float *delta, void *dk, void *dv, const DkvSplit &sp, float *part, int B,
              int H, int Hkv, int N, int d, int dtype, float scale, int causal,
-             const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
+             const uint8_t *mask, const fa::DropSpec &drop, bool after_dq, void *stream) {
     fa::Maps maps;
     fa::BwdParams p;
     int rc = bwd_params(q, k, v, dout, lse, delta, B, H, Hkv, N, d, dtype, scale, causal, mask,
@@ -310,7 +311,7 @@ int run_dkdv(const void *q, const void *k, const void *v, const void *dout, cons
         maps.out1 = maps.v;
     }
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fa::launch_bwd_dkdv(maps, p, d, dtype == FA_BF16, st);
+    cudaError_t e = fa::launch_bwd_dkdv(maps, p, d, dtype == FA_BF16, after_dq, st);
     if (e == cudaSuccess && sp.splits > 1)
         e = fa::launch_bwd_group_reduce(part, dk, dv, sp.splits, p.kv_elems, dtype == FA_BF16, st);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -348,15 +349,26 @@ int run_preprocess(const void *o, const void *dout, float *delta, int B, int H, 
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// The whole backward: D, dK/dV (+ reduce), dQ.  delta: B*H*N floats; sp, part: see run_dkdv.
+// The whole backward: D, then dQ and dK/dV.  delta: B*H*N floats; sp, part: see run_dkdv.
+// The two passes read the same inputs and write disjoint outputs, so with one dK/dV split the
+// dK/dV grid is queued after the dQ grid with programmatic stream serialization: its CTAs fill
+// the SMs that the dQ grid's last wave leaves idle.  Split K/V groups keep the plain order
+// dK/dV, group reduce, dQ.
 int run_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
             const float *lse, void *dq, void *dk, void *dv, float *delta, const DkvSplit &sp,
             float *part, int B, int H, int Hkv, int N, int d, int dtype, float scale, int causal,
             const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
     int rc = run_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
     if (rc != FA_OK) return rc;
+    if (sp.splits == 1) {
+        rc = run_dq(q, k, v, dout, lse, delta, dq, B, H, Hkv, N, d, dtype, scale, causal, mask,
+                    drop, stream);
+        if (rc != FA_OK) return rc;
+        return run_dkdv(q, k, v, dout, lse, delta, dk, dv, sp, part, B, H, Hkv, N, d, dtype,
+                        scale, causal, mask, drop, true, stream);
+    }
     rc = run_dkdv(q, k, v, dout, lse, delta, dk, dv, sp, part, B, H, Hkv, N, d, dtype, scale,
-                  causal, mask, drop, stream);
+                  causal, mask, drop, false, stream);
     if (rc != FA_OK) return rc;
     return run_dq(q, k, v, dout, lse, delta, dq, B, H, Hkv, N, d, dtype, scale, causal, mask,
                   drop, stream);
@@ -491,7 +503,7 @@ int fa_bwd_dkdv(const void *q, const void *k, const void *v, const void *dout, c
                 const float *delta, void *dk, void *dv, int B, int H, int N, int d, int dtype,
                 float scale, int causal, const uint8_t *block_mask, void *stream) {
     return run_dkdv(q, k, v, dout, lse, delta, dk, dv, DkvSplit{1, 1}, nullptr, B, H, H, N, d,
-                    dtype, scale, causal, block_mask, kNoDrop, stream);
+                    dtype, scale, causal, block_mask, kNoDrop, false, stream);
 }
 
 int fa_bwd_dq(const void *q, const void *k, const void *v, const void *dout, const float *lse,
@@ -679,6 +691,8 @@ const char *fa_status_string(int code) {
 }
 
 int fa_debug_set_visit_log(uint8_t *buf, size_t bytes) {
+    if (bytes != 0 && (buf == nullptr || (reinterpret_cast<uintptr_t>(buf) & 3u) != 0))
+        return FA_ERR_INVALID;
     std::lock_guard<std::mutex> lk(g_mu);
     g_visit_log = bytes ? buf : nullptr;
     g_visit_bytes = bytes;

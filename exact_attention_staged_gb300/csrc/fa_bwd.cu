@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             };
             auto log_visit = [&](int hq, int i) {
                 if (p.ctl.visit_log != nullptr && lane == 0)
-                    p.ctl.visit_log[(static_cast<size_t>(hq) * p.T + i) * p.T + kt] |= 2;
+                    visit_mark(p.ctl.visit_log, (static_cast<size_t>(hq) * p.T + i) * p.T + kt, 2u);
             };
             bool ok = mbar_wait_warp(kv_full, 0, p.ctl, abort_flag);
             int hq = hq0, i = i0 - 1;
@@ -555,6 +555,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // Launched to overlap the tail of the dQ pass (see launch_dkdv_t), this grid must not
+    // complete before that pass has: whatever the caller queues next may overwrite what dQ reads.
+    if (threadIdx.x == 0) griddep_wait();
 }
 
 // ================================================================================ dQ
@@ -652,6 +655,9 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the dK/dV pass queued after this one reads nothing it writes: let it take the SMs that
+    // this grid's last CTAs leave idle
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -732,7 +738,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         issue_ss(tmem, dQa, 0);
                         umma_commit_el(&s_full[0]);
                         if (p.ctl.visit_log != nullptr && lane == 0)
-                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j] |= 4;
+                            visit_mark(p.ctl.visit_log, (static_cast<size_t>(bh) * p.T + qt) * p.T + j, 4u);
                     }
                     if (ok && j1 < jend) {
                         ok = full_wait(2);
@@ -741,7 +747,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                             issue_ss(tmem + 128, dQa, 2);
                             umma_commit_el(&s_full[1]);
                             if (p.ctl.visit_log != nullptr && lane == 0)
-                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j1] |= 4;
+                                visit_mark(p.ctl.visit_log, (static_cast<size_t>(bh) * p.T + qt) * p.T + j1, 4u);
                         }
                     }
                 }
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                         issue_ss(buf, dQa, 2 * n + 4);
                         umma_commit_el(&s_full[n & 1]);
                         if (p.ctl.visit_log != nullptr && lane == 0)
-                            p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + qt) * p.T + j2] |= 4;
+                            visit_mark(p.ctl.visit_log, (static_cast<size_t>(bh) * p.T + qt) * p.T + j2, 4u);
                     }
                     j = j1;
                     j1 = j2;
@@ -980,17 +986,29 @@ cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long row
     return cudaGetLastError();
 }
 
+// after_dq: the launch directly follows the dQ pass of the same backward call on `stream`; it is
+// made with programmatic stream serialization, so its CTAs start on the SMs the dQ grid's last
+// CTAs leave idle (the two passes share no output; every CTA of this grid waits for the dQ grid
+// before it exits).
 template <int D, bool BF16>
-cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, cudaStream_t stream) {
+cudaError_t launch_dkdv_t(const Maps &m, const BwdParams &p, bool after_dq, cudaStream_t stream) {
     using L = DkvLayout<D>;
     auto kern = p.drop.t4 != 0 ? fa_bwd_dkdv_kernel<D, BF16, true>
                                : fa_bwd_dkdv_kernel<D, BF16, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(static_cast<long>(p.units) * p.T), L::kThreads, L::kAlloc,
-           stream>>>(m.q, m.k, m.v, m.dout, m.out0, m.out1, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(p.units) * p.T));
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_dq ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.dout, m.out0, m.out1, p);
 }
 
 template <int D, bool BF16>
@@ -1028,11 +1046,11 @@ cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int s
 }
 
 cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf16,
-                            cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_dkdv_t<64, true>(maps, p, stream)
-                             : launch_dkdv_t<64, false>(maps, p, stream);
-    return bf16 ? launch_dkdv_t<128, true>(maps, p, stream)
-                : launch_dkdv_t<128, false>(maps, p, stream);
+                            bool after_dq, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_dkdv_t<64, true>(maps, p, after_dq, stream)
+                             : launch_dkdv_t<64, false>(maps, p, after_dq, stream);
+    return bf16 ? launch_dkdv_t<128, true>(maps, p, after_dq, stream)
+                : launch_dkdv_t<128, false>(maps, p, after_dq, stream);
 }
 
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,

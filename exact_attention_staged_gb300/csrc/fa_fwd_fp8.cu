@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(384, 1)
                             issue_s(t, ks);
                             umma_commit_el(&s_full[t]);
                             if (p.ctl.visit_log != nullptr && lane == 0)
-                                p.ctl.visit_log[(static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T +
-                                                j] |= 1;
+                                visit_mark(p.ctl.visit_log,
+                                           (static_cast<size_t>(bh) * p.T + (qt0 + t)) * p.T + j, 1u);
                         }
                     }
                     if (!ok) break;

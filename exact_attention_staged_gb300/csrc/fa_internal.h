@@ -50,6 +50,14 @@ __device__ __forceinline__ bool tile_live(const Params &p, const uint32_t *rowbi
     return p.T <= kMaskSmemTiles ? mask_bit(rowbits, j) : p.mask[qt * p.T + j] != 0;
 }
 
+// Test hook: OR `bit` into byte `idx` of the tile-visit log, atomically on the containing 32-bit
+// word (the log is 4-byte aligned): the dQ and dK/dV passes of one backward call may run at the
+// same time and mark neighbouring bytes.
+__device__ __forceinline__ void visit_mark(uint8_t *log, size_t idx, uint32_t bit) {
+    atomicOr(reinterpret_cast<unsigned int *>(log + (idx & ~static_cast<size_t>(3))),
+             bit << (8 * (idx & 3)));
+}
+
 // CTA order: heads are taken in groups of `group` so that the tiles streamed by the CTAs that
 // run at the same time (K/V of the forward, Q/dO of dK/dV, K/V of dQ) stay within a slice of
 // L2; inside a group the work unit (query-tile pair or tile) advances slowest, longest first.
@@ -153,7 +161,7 @@ cudaError_t launch_fwd(const Maps &maps, const FwdParams &p, int d, bool bf16,
 cudaError_t launch_bwd_preprocess(const void *o, const void *dout, float *delta, long rows,
                                   int d, bool bf16, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf16,
-                            cudaStream_t stream);
+                            bool after_dq, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
                           cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream);

@@ -549,6 +549,18 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  launch_dependents: this CTA no longer
+// holds back the grid launched after it with programmatic stream serialization (that grid starts
+// once every CTA of this one has signalled or exited).  wait: block until the grids this one was
+// allowed to overlap have completed and their memory operations are visible; returns at once
+// for a grid launched without that attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

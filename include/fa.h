@@ -256,7 +256,8 @@ const char *fa_status_string(int code);
  * fa_debug_set_visit_log: when buf != NULL, every kernel ORs a bit into
  *   buf[((b*H + h) * T + i) * T + j] for each score tile (query tile i, key tile j) it
  *   computes: bit 0 forward, bit 1 dK/dV, bit 2 dQ.  bytes must cover B*H*T*T of the launches
- *   that follow.  NULL turns logging off.
+ *   that follow, rounded up to a multiple of 4 (the bits are set by 32-bit atomic ORs); buf
+ *   must be 4-byte aligned (otherwise FA_ERR_INVALID).  NULL (or bytes = 0) turns logging off.
  * fa_debug_set_wait_limit_ns: bound on every device pipeline wait (default 2 s; 0 restores it).
  * fa_debug_set_fault: 0 = none; 1 = the forward's load warp skips the first key tile of each
  *   CTA; 2 = the dK/dV pass's load warp skips its first Q tile; 3 = the dQ pass's load warp

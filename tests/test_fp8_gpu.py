@@ -26,7 +26,7 @@ import torch
 import oracle
 from exact_attention_staged_gb300.workloads import (BLOCK, FP8_WORKLOADS, fp8_workload_inputs,
                                                     make_block_mask, make_fp8_inputs)
-from test_parity_gpu import DEV, expected_visits, np64, relf
+from test_parity_gpu import DEV, expected_visits, np64, relf, visit_log_buffer
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,7 @@ def test_fp8_block_sparse_visits_and_dead_rows(cuda_lib, record_property):
     mask = make_block_mask(T, 23, 0.4)
     mask[3, :] = 0
     t = make_fp8_inputs(1, 2, N, d, seed=640, qk_mult=2.0)
-    log = torch.zeros(2 * T * T, dtype=torch.uint8, device=DEV)
+    log = visit_log_buffer(2 * T * T)
     cuda_lib.debug_set_visit_log(log)
     try:
         o, lse = run_fp8(cuda_lib, t, 0.1, True, mask)
@@ -100,7 +100,7 @@ def test_fp8_block_sparse_visits_and_dead_rows(cuda_lib, record_property):
     vmax = float(np.max(np.abs(oracle.e4m3_to_f64(t["v"])))) * t["descale_v"]
     check_fp8(o, lse, ref, vmax, "fp8 sparse", record_property)
     assert torch.all(o[:, :, 384:512].cpu() == 0)
-    got = log.cpu().numpy().reshape(2, T, T)
+    got = log.cpu().numpy()[:2 * T * T].reshape(2, T, T)
     assert np.array_equal(got, expected_visits(2, T, True, mask) & 1)
 
 

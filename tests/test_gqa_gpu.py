@@ -12,7 +12,7 @@ import torch
 import oracle
 from exact_attention_staged_gb300.workloads import (BLOCK, WORKLOADS, make_block_mask,
                                                     make_inputs, workload_inputs)
-from test_parity_gpu import DEV, check_bwd, check_fwd, expected_visits, np64
+from test_parity_gpu import DEV, check_bwd, check_fwd, expected_visits, np64, visit_log_buffer
 
 pytestmark = pytest.mark.gpu
 
@@ -83,7 +83,7 @@ def test_gqa_tile_visits_and_determinism(cuda_lib, splits):
     B, H, Hkv, N, d = 1, 6, 2, 700, 64
     T = (N + BLOCK - 1) // BLOCK
     t = make_inputs(B, H, N, d, torch.bfloat16, seed=430, h_kv=Hkv)
-    log = torch.zeros(B * H * T * T, dtype=torch.uint8, device=DEV)
+    log = visit_log_buffer(B * H * T * T)
     cuda_lib.debug_set_dkdv_splits(splits)
     cuda_lib.debug_set_visit_log(log)
     try:
@@ -94,7 +94,7 @@ def test_gqa_tile_visits_and_determinism(cuda_lib, splits):
         second = run_gqa(cuda_lib, t, 0.125, True)
     finally:
         cuda_lib.debug_set_dkdv_splits(0)
-    got = log.cpu().numpy().reshape(B * H, T, T)
+    got = log.cpu().numpy()[:B * H * T * T].reshape(B * H, T, T)
     assert np.array_equal(got, expected_visits(B * H, T, True, None))
     for x, y in zip(first[2], second[2]):
         assert torch.equal(x, y)

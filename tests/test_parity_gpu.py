@@ -126,6 +126,12 @@ def test_block_mask_wider_than_shared_copy(cuda_lib, T):
         check_bwd([g[0, 0, rows] for g in grads], ref, f"T={T} block {a}")
 
 
+def visit_log_buffer(n):
+    """A zeroed device log for n tile entries, rounded up to whole 32-bit words (the kernels mark
+    it with 32-bit atomic ORs)."""
+    return torch.zeros((n + 3) // 4 * 4, dtype=torch.uint8, device=DEV)
+
+
 def expected_visits(BH, T, causal, mask):
     i = np.arange(T)
     live = np.ones((T, T), dtype=bool)
@@ -143,13 +149,13 @@ def test_tile_skipping_is_bit_exact(cuda_lib, causal, sparse):
     T = (N + BLOCK - 1) // BLOCK
     mask = make_block_mask(T, 9, 0.3) if sparse else None
     t = make_inputs(B, H, N, d, torch.bfloat16, seed=9)
-    log = torch.zeros(B * H * T * T, dtype=torch.uint8, device=DEV)
+    log = visit_log_buffer(B * H * T * T)
     cuda_lib.debug_set_visit_log(log)
     try:
         run_pair(cuda_lib, t, 0.125, causal, mask)
     finally:
         cuda_lib.debug_set_visit_log(None)
-    got = log.cpu().numpy().reshape(B * H, T, T)
+    got = log.cpu().numpy()[:B * H * T * T].reshape(B * H, T, T)
     assert np.array_equal(got, expected_visits(B * H, T, causal, mask))
 
 
