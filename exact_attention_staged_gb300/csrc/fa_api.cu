@@ -132,10 +132,12 @@ int make_map_bytes(CUtensorMap *m, const void *base, long x, long y, long z, int
 int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 
 // Dropout decisions: drop probability p -> byte threshold t = nearest integer to 256 p (ties to
-// even), valid for 0 <= t <= 255; t = 0 turns dropout off.
+// even), valid for 0 <= t <= 255; t = 0 turns dropout off.  The offset is a 32-bit counter word
+// of the generator.
 constexpr fa::DropSpec kNoDrop = {0u, 1.f, 0ull, 0ull};
 int make_drop(float p, unsigned long long seed, unsigned long long offset, fa::DropSpec *out) {
     if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID;
+    if (offset > 0xFFFFFFFFull) return FA_ERR_INVALID;  // a 32-bit counter word
     const long t = std::lrint(static_cast<double>(p) * 256.0);
     if (t < 0 || t > 255) return FA_ERR_INVALID;
     out->t4 = static_cast<uint32_t>(t) * 0x01010101u;

@@ -160,9 +160,10 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
  * operations fused into the kernel, O = dropout(softmax(S)) V; the pages give no generator).
  * Score (q, k) of query head b*H + h is dropped with probability t / 256, t = the nearest
  * integer to 256 * p_drop (ties to even), and a kept probability is scaled by 256 / (256 - t).
- * The decision is byte (k mod 32) of Philox4x64-10 (Salmon et al., SC 2011) with counter
- * (k div 32, q, b*H + h, 0) and key (seed, offset), kept when that byte is >= t; the backward
- * regenerates the same decisions from the same arguments, so nothing is stored.
+ * The decision is byte (k mod 16) of Philox4x32-10 (Salmon et al., SC 2011) with counter
+ * (k div 16, q, b*H + h, offset) and key (seed mod 2^32, seed div 2^32), kept when that byte is
+ * >= t; the backward regenerates the same decisions from the same arguments, so nothing is
+ * stored.  offset must be below 2^32 (otherwise FA_ERR_INVALID).
  * fa_fwd_dropout: as fa_fwd_gqa; LSE is that of the scores (dropout does not change it).
  * fa_bwd_dropout: as fa_bwd_gqa (same workspace) for the forward with these dropout arguments.
  *   p_drop : 0 <= p_drop < 1 with t <= 255 (otherwise FA_ERR_INVALID); t = 0 is no dropout.

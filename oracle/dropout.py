@@ -5,14 +5,16 @@ The FlashAttention paper detail page lists dropout among the operations fused in
 attention kernel (O = dropout(softmax(S)) V), and the FlashAttention-2 reading notes keep it in
 the backward; neither page fixes a random-number generator.  The reading taken here:
 
-* Generator: Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
-  1, 2, 3", SC 2011): a 256-bit counter and a 128-bit key, ten rounds of two 64 x 64 -> 128-bit
-  multiplications, with the key bumped by two Weyl constants between rounds.  It is pinned
-  against numpy's ``np.random.Philox`` (the same generator) in the tests.
-* Decisions: score (q, k) of head bh (b * H + h) takes byte (k mod 32) of the 32 output bytes
-  (4 little-endian 64-bit words) of Philox4x64-10 with counter (k div 32, q, bh, 0) and key
-  (seed, offset); it is dropped when that byte is below t = nearest integer to 256 p (ties to
-  even), so the drop probability is t / 256, and kept probabilities are scaled by 256 / (256 - t).
+* Generator: Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+  1, 2, 3", SC 2011): a 128-bit counter of four 32-bit words and a 64-bit key, ten rounds of two
+  32 x 32 -> 64-bit multiplications whose halves are swapped and xored into the other words,
+  with the key bumped by two Weyl constants between rounds.  It is pinned in the tests against
+  cuRAND's host Philox4_32_10 generator (an independent implementation of the same generator).
+* Decisions: score (q, k) of head bh (b * H + h) takes byte (k mod 16) of the 16 output bytes
+  (4 little-endian 32-bit words) of Philox4x32-10 with counter (k div 16, q, bh, offset) and key
+  (seed mod 2^32, seed div 2^32); it is dropped when that byte is below t = nearest integer to
+  256 p (ties to even), so the drop probability is t / 256, and kept probabilities are scaled by
+  256 / (256 - t).  The offset is below 2^32.
 * Forward: P = softmax(S) (masked as usual), P_d = P o Z * 256 / (256 - t), O = P_d V; LSE is the
   logsumexp of the scores (dropout does not change it).
 * Backward: dV = P_d^T dO, dP = (dO V^T) o Z * 256 / (256 - t), D = rowsum(P o dP)
@@ -24,35 +26,27 @@ import numpy as np
 
 from . import _f64, probabilities
 
-_M0, _M1 = np.uint64(0xD2E7470EE14C6C93), np.uint64(0xCA5A826395121157)
-_W0, _W1 = np.uint64(0x9E3779B97F4A7C15), np.uint64(0xBB67AE8584CAA73B)
+_M0, _M1 = np.uint64(0xD2511F53), np.uint64(0xCD9E8D57)  # round multipliers
+_W0, _W1 = np.uint64(0x9E3779B9), np.uint64(0xBB67AE85)  # key increments (Weyl constants)
 _LO = np.uint64(0xFFFFFFFF)
 _S32 = np.uint64(32)
 
 
-def _mulhilo(a: np.uint64, b: np.ndarray):
-    """(high, low) 64-bit halves of the 128-bit products a * b, from 32-bit partial products."""
-    a_lo, a_hi = a & _LO, a >> _S32
-    b_lo, b_hi = b & _LO, b >> _S32
-    ll, lh, hl, hh = a_lo * b_lo, a_lo * b_hi, a_hi * b_lo, a_hi * b_hi
-    mid = (ll >> _S32) + (lh & _LO) + (hl & _LO)
-    lo = (ll & _LO) | ((mid & _LO) << _S32)
-    hi = hh + (lh >> _S32) + (hl >> _S32) + (mid >> _S32)
-    return hi, lo
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32-10 of counters [..., 4] (32-bit words) under key (k0, k1): [..., 4] uint32.
 
-
-def philox4x64_10(counter, key) -> np.ndarray:
-    """Philox4x64-10 of counters [..., 4] (uint64) under key (k0, k1): [..., 4] uint64."""
-    c = np.asarray(counter, dtype=np.uint64)
+    Each round multiplies counter words 0 and 2 by the two multipliers (a 32 x 32 -> 64-bit
+    product, exact in uint64); the new words are (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2),
+    hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); then the key words advance by the Weyl constants (mod 2^32).
+    """
+    c = np.asarray(counter, dtype=np.uint64) & _LO
     c0, c1, c2, c3 = (c[..., i].copy() for i in range(4))
-    k0, k1 = np.uint64(key[0]), np.uint64(key[1])
-    with np.errstate(over="ignore"):
-        for _ in range(10):
-            hi0, lo0 = _mulhilo(_M0, c0)
-            hi1, lo1 = _mulhilo(_M1, c2)
-            c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
-            k0, k1 = k0 + _W0, k1 + _W1
-    return np.stack([c0, c1, c2, c3], axis=-1)
+    k0, k1 = np.uint64(int(key[0]) & 0xFFFFFFFF), np.uint64(int(key[1]) & 0xFFFFFFFF)
+    for _ in range(10):
+        p0, p1 = _M0 * c0, _M1 * c2
+        c0, c1, c2, c3 = (p1 >> _S32) ^ c1 ^ k0, p1 & _LO, (p0 >> _S32) ^ c3 ^ k1, p0 & _LO
+        k0, k1 = (k0 + _W0) & _LO, (k1 + _W1) & _LO
+    return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
 
 
 def threshold(p: float) -> int:
@@ -65,12 +59,14 @@ def threshold(p: float) -> int:
 
 def keep_mask(bh: int, Nq: int, Nk: int, seed: int, offset: int, t: int) -> np.ndarray:
     """keep[q, k] (bool) for every score of head bh."""
-    nkb = (Nk + 31) // 32
+    if not 0 <= offset < 2 ** 32:
+        raise ValueError("the dropout offset is a 32-bit counter word")
+    nkb = (Nk + 15) // 16
     q, kb = np.meshgrid(np.arange(Nq, dtype=np.uint64), np.arange(nkb, dtype=np.uint64),
                         indexing="ij")
-    ctr = np.stack([kb, q, np.full_like(q, bh), np.zeros_like(q)], axis=-1)
-    words = philox4x64_10(ctr, (seed, offset))                   # [Nq, nkb, 4]
-    b = words.astype("<u8").view(np.uint8).reshape(Nq, nkb * 32)  # byte k mod 32 of block k div 32
+    ctr = np.stack([kb, q, np.full_like(q, bh), np.full_like(q, offset)], axis=-1)
+    words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, seed >> 32))   # [Nq, nkb, 4]
+    b = words.astype("<u4").view(np.uint8).reshape(Nq, nkb * 16)  # byte k mod 16 of block k div 16
     return b[:, :Nk] >= t
 
 

@@ -97,6 +97,16 @@ def test_host_validation_rejects_before_launch(lib):
                       None) == api.FA_ERR_INVALID  # workspace too small
     assert lib.fa_debug_set_fault(5) == api.FA_ERR_INVALID
     assert lib.fa_debug_set_fault(-1) == api.FA_ERR_INVALID
+    # dropout: p outside [0, 1) and offsets that do not fit the generator's 32-bit counter word
+    assert lib.fa_fwd_dropout(p, p, p, p, p, 1, 1, 1, 128, 64, 1, 0.125, 0, None, 1.0, 1, 0,
+                              None) == api.FA_ERR_INVALID
+    assert lib.fa_fwd_dropout(p, p, p, p, p, 1, 1, 1, 128, 64, 1, 0.125, 0, None, 0.1, 1,
+                              1 << 32, None) == api.FA_ERR_INVALID
+    assert lib.fa_bwd_dropout(p, p, p, p, p, p, p, p, p, p, 1 << 20, 1, 1, 1, 128, 64, 1, 0.125,
+                              0, None, 0.1, 1, 1 << 32, None) == api.FA_ERR_INVALID
+    # the tile-visit log must be 4-byte aligned (its marks are 32-bit atomic ORs)
+    assert lib.fa_debug_set_visit_log(ctypes.c_void_p(18), 64) == api.FA_ERR_INVALID
+    assert lib.fa_debug_set_visit_log(None, 0) == api.FA_OK
 
 
 def test_missing_library_fails_loudly(tmp_path):

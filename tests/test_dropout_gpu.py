@@ -1,5 +1,5 @@
 """GPU parity of attention with dropout (fa_fwd_dropout, fa_bwd_dropout) against the fp64
-oracle (``oracle.dropout``), which draws the same Philox4x64-10 decisions independently.
+oracle (``oracle.dropout``), which draws the same Philox4x32-10 decisions independently.
 
 Tolerances as in test_parity_gpu: dropout only zeroes probabilities and scales the rest by
 256 / (256 - t), so the rounding behaviour of O and the gradients is that of the plain path.
@@ -63,6 +63,13 @@ def test_dropout_block_sparse_and_seed_dependence(cuda_lib):
     assert torch.equal(o, o2) and all(torch.equal(a, b) for a, b in zip(grads, g2))
     o3, lse3, _ = run_drop(cuda_lib, t, 0.1, True, 0.2, 99, 4, mask)
     assert not torch.equal(o, o3) and torch.equal(lse, lse3)
+    # a seed above 2^32 fills both key words of the generator; the largest 32-bit offset
+    seed, off = 0xDEADBEEF12345678, 2 ** 32 - 1
+    o4, lse4, g4 = run_drop(cuda_lib, t, 0.1, True, 0.2, seed, off, mask)
+    ref4 = odrop.attention_dropout(t["q"], t["k"], t["v"], 0.1, 0.2, seed, off, True, mask,
+                                   dout=t["do"])
+    check_fwd(o4, lse4, ref4, "dropout 64-bit seed")
+    check_bwd(g4, ref4, "dropout 64-bit seed")
 
 
 def test_dropout_zero_probability_is_the_plain_path(cuda_lib):

@@ -530,17 +530,54 @@ def test_fp8_descales_in_a_two_key_closed_form():
 from oracle import dropout as odrop  # noqa: E402
 
 
-def test_philox_matches_numpy_generator():
-    # numpy's Philox is the same Philox4x64-10; its stream advances the counter before each
-    # block, so the block of counter c + 1 comes first
-    for ctr, key in (((5, 0, 0, 0), (12345, 678)), ((0, 7, 3, 0), (2 ** 63 + 5, 1)),
-                     ((123456789, 42, 9, 0), (0, 0))):
-        bg = np.random.Philox(counter=np.array(ctr, dtype=np.uint64),
-                              key=np.array(key, dtype=np.uint64))
-        raw = bg.random_raw(8)
-        c = np.array([[ctr[0] + 1, *ctr[1:]], [ctr[0] + 2, *ctr[1:]]], dtype=np.uint64)
-        mine = odrop.philox4x64_10(c, key).reshape(-1)
-        np.testing.assert_array_equal(mine, raw)
+def _curand():
+    """cuRAND (an NVIDIA library with its own Philox4x32-10) through ctypes, or None."""
+    import ctypes
+    import ctypes.util
+    names = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcurand.so"),
+             ctypes.util.find_library("curand"), "libcurand.so", "libcurand.so.10"]
+    for n in names:
+        if not n:
+            continue
+        try:
+            return ctypes.CDLL(n)
+        except OSError:
+            continue
+    return None
+
+
+def _curand_philox_words(lib, seed, offset, n):
+    import ctypes
+    gen = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), 161) == 0  # PSEUDO_PHILOX4_32_10
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(offset)) == 0
+        out = np.zeros(n, dtype=np.uint32)
+        assert lib.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(n)) == 0
+    finally:
+        lib.curandDestroyGenerator(gen)
+    return out
+
+
+def test_philox_matches_curand_host_generator():
+    # cuRAND's host Philox4_32_10 generator is another implementation of the same generator:
+    # for seed s its value 4 i + j is word j of Philox4x32-10 with counter (0, 0, i, 0) and key
+    # (s mod 2^32, s div 2^32), so whole blocks, every round and the key schedule are compared
+    lib = _curand()
+    if lib is None:
+        pytest.skip("cuRAND is not installed")
+    for seed in (0, 1, 0x123456789ABCDEF0, 2 ** 64 - 1):
+        ref = _curand_philox_words(lib, seed, 0, 256).reshape(64, 4)
+        ctr = np.zeros((64, 4), dtype=np.uint64)
+        ctr[:, 2] = np.arange(64)
+        mine = odrop.philox4x32_10(ctr, (seed & 0xFFFFFFFF, seed >> 32))
+        np.testing.assert_array_equal(mine, ref)
+    # a start offset lands on block offset / 4 of the same stream
+    ref = _curand_philox_words(lib, 77, 4 * 1000, 8).reshape(2, 4)
+    ctr = np.zeros((2, 4), dtype=np.uint64)
+    ctr[:, 2] = [1000, 1001]
+    np.testing.assert_array_equal(odrop.philox4x32_10(ctr, (77, 0)), ref)
 
 
 def test_dropout_rate_and_threshold():
