@@ -88,6 +88,9 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, const void *dout,
                                                                 float *delta, long rows) {
     constexpr int kLanes = D / 8;  // 8 elements (16 bytes) per lane
+    // queued right after the forward with programmatic stream serialization: O is complete and
+    // visible only past this point
+    griddep_wait();
     const long gid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long row = gid / kLanes;
     const int part = static_cast<int>(gid % kLanes);
@@ -976,14 +979,24 @@ __global__ void __launch_bounds__(256) fa_bwd_group_reduce_kernel(const float *p
     reinterpret_cast<uint4 *>(static_cast<elem_t<BF16> *>(which ? dv : dk) + e)[0] = w;
 }
 
+// Launched with programmatic stream serialization: when the forward kernel is the grid queued
+// just before (the usual order, forward then backward), this small kernel's CTAs are scheduled
+// beside its last CTAs instead of after its completion; it waits for that grid before reading.
 template <int D, bool BF16>
 cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long rows,
                          cudaStream_t stream) {
     const long threads = rows * (D / 8);
     const long blocks = (threads + 255) / 256;
-    fa_bwd_preprocess_kernel<D, BF16>
-        <<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o, dout, delta, rows);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_bwd_preprocess_kernel<D, BF16>, o, dout, delta, rows);
 }
 
 // after_dq: the launch directly follows the dQ pass of the same backward call on `stream`; it is

@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     };
 #pragma unroll
     for (int t = 0; t < kStages - 1; ++t) load_tile(t);
+    // the range merge queued after this grid may take its SM slots early (it waits for this
+    // grid's completion before it reads a partial result)
+    if (tid == 0) griddep_launch_dependents();
 
     const T *qrows = reinterpret_cast<const T *>(p.q) + static_cast<size_t>(grow0) * D;
     for (int i = tid; i < RPC * D; i += kThreads)
@@ -316,6 +319,9 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
     const long row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // launched to overlap the tail of the range kernel: its partial results are complete and
+    // visible only past this point
+    griddep_wait();
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
     // every warp finds M over all ranges, 32 at a time, lane s holding range s
     float M = -INFINITY;
@@ -409,9 +415,18 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     else if (rpc <= 8) e = launch_decode_rpc<D, BF16, 8>(p, stream);
     else e = launch_decode_rpc<D, BF16, 16>(p, stream);
     if (e != cudaSuccess || p.splits == 1) return e;
-    const long rows = static_cast<long>(p.B) * p.H * p.Nq;
-    fa_decode_combine_kernel<D, BF16><<<static_cast<unsigned>(rows), 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    // programmatic stream serialization: the merge's CTAs (small: 128 threads, 2 KB) are
+    // scheduled beside the range kernel's last CTAs instead of after its completion
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long>(p.B) * p.H * p.Nq));
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<D, BF16>, p);
 }
 
 }  // namespace

@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // a backward pre-pass queued after this grid with programmatic stream serialization may
+    // start on the SMs this grid's last CTAs leave idle; it waits for this grid before reading
+    if (threadIdx.x == 0) griddep_launch_dependents();
     // warpgroup 0 (load warp, MMA warp, two idle warps) gives registers to the two softmax
     // warpgroups: 128 x 64 + 256 x 216 = 63488 of the 384 x 168 = 64512 the CTA is launched with
     if (warp < 4) {
