@@ -96,13 +96,14 @@ int check_ptrs(std::initializer_list<const void *> ptrs) {
     return FA_OK;
 }
 
-// [B*H, N, d] 16-bit tensor, 64 x 128 boxes (128 bytes x 128 rows), 128-byte swizzle.
-int make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int dtype) {
+// [B*H, N, d] 16-bit tensor, 64 x box_rows boxes (128 bytes x box_rows rows), 128-byte swizzle.
+int make_map(CUtensorMap *m, const void *base, int BH, int N, int d, int dtype,
+             int box_rows = 128) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m,
                           dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -663,7 +664,13 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
     p.chunk = sp.chunk;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
-    cudaError_t e = fa::launch_decode(p, d, dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+    if (make_ctl(status, 0, 0, &p.ctl) != FA_OK) return FA_ERR_INVALID;
+    fa::DecodeMaps maps;
+    if (make_map(&maps.k, k, B * H_kv, Nk, d, dtype, 16) ||
+        make_map(&maps.v, v, B * H_kv, Nk, d, dtype, 16))
+        return FA_ERR_CUDA;
+    cudaError_t e = fa::launch_decode(maps, p, d, dtype == FA_BF16,
+                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -13,9 +13,11 @@
 // GB300 mapping: no tensor cores (one to sixteen rows per key: 4 to 64 FLOP per 16-bit K/V
 // element pair, far below what would make the MMA pipe the limit); 128 threads per CTA, seven
 // CTAs per SM at up to four rows (each CTA's tile loop is a chain of barriers and shuffles, so
-// resident CTAs set the rate).  K and V tiles of 16 keys stream through a three-stage cp.async
-// ring (K rows padded to 272 or 144 bytes, so 16-byte reads of 8 consecutive rows hit distinct
-// banks).  Per tile:
+// resident CTAs set the rate).  K and V tiles of 16 keys stream through a three-stage ring
+// filled by TMA (one thread issues a tile's boxes; completion on the stage's mbarrier), in boxes
+// of 64 elements x 16 keys with the 128-byte swizzle: 16-byte chunk c of key row r sits at
+// chunk position c ^ (r mod 8), so the 16-byte reads of 8 consecutive key rows (phase A) and the
+// 128-byte row reads (phase B) are free of bank conflicts without padding.  Per tile:
 //   A   every warp takes a quarter of d, every lane one key and half of that quarter: partial
 //       dot products of that key with all rows (query rows broadcast from shared memory, fp32,
 //       pre-scaled by scale * log2 e), the two halves summed by one shuffle;
@@ -42,20 +44,25 @@ constexpr int kStages = 3;    // K/V tiles in the cp.async ring (two in flight w
 
 template <int D, int RPC>
 struct DecLayout {
-    // K rows padded by 16 bytes (phase A reads 16 bytes of 8 consecutive rows at once); V rows
-    // not (phase B reads 128 contiguous bytes of one row per warp)
-    static constexpr int kKRowBytes = D * 2 + 16;
-    static constexpr int kVRowBytes = D * 2;
-    static constexpr int kKTileBytes = kKeys * kKRowBytes;
-    static constexpr int kVTileBytes = kKeys * kVRowBytes;
-    static constexpr int kQOff = 0;                                 // float [RPC][D]
-    static constexpr int kKOff = kQOff + RPC * D * 4;               // kStages tiles
-    static constexpr int kVOff = kKOff + kStages * kKTileBytes;     // kStages tiles
-    static constexpr int kPartOff = kVOff + kStages * kVTileBytes;  // float [4][RPC][kKeys]
+    static constexpr int kBoxBytes = kKeys * 128;                   // 64 elements x 16 keys
+    static constexpr int kTileBytes = kKeys * D * 2;                // D / 64 boxes
+    static constexpr int kKOff = 0;                                 // kStages tiles (1024-aligned)
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;      // kStages tiles
+    static constexpr int kQOff = kVOff + kStages * kTileBytes;      // float [RPC][D]
+    static constexpr int kPartOff = kQOff + RPC * D * 4;            // float [4][RPC][kKeys]
     static constexpr int kPOff = kPartOff + 4 * RPC * kKeys * 4;    // float [RPC][kKeys]
     static constexpr int kStatOff = kPOff + RPC * kKeys * 4;        // alpha, m, l [RPC] each
-    static constexpr int kBytes = kStatOff + 3 * RPC * 4;
+    static constexpr int kBarOff = (kStatOff + 3 * RPC * 4 + 7) / 8 * 8;  // full[kStages]
+    static constexpr int kAbortOff = kBarOff + kStages * 8;
+    static constexpr int kBytes = kAbortOff + 8;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
 };
+
+// Byte offset of the 16-byte chunk holding elements [8 c, 8 c + 8) of key row r in a tile of
+// 128-byte-swizzled 64-element boxes.
+__device__ __forceinline__ int swz_chunk(int r, int c) {
+    return (c >> 3) * (kKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
 template <bool BF16>
 using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
@@ -75,7 +82,9 @@ __device__ __forceinline__ float half_sum(float v) {
 
 // RPC: query rows per CTA (1, 2, 4, 8 or 16), the smallest that holds a K/V head's rows.
 template <int D, bool BF16, int RPC>
-__global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const DecodeParams p) {
     using L = DecLayout<D, RPC>;
     using T = elem_t<BF16>;
     constexpr int kPairs = D / 2;                 // column pairs of O
@@ -83,14 +92,16 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     constexpr int kKeysB = kKeys / kRB;           // keys per group and tile (16 or 8)
     constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in the final merge and store
     static_assert(kKeysB % 4 == 0, "probabilities are read four keys at a time");
-    static_assert(kRB * RPC * D * 4 <= L::kPOff,
-                  "the merge buffer reuses the query rows, the K/V ring and the partial dots");
+    static_assert(kRB * RPC * D * 4 <= L::kBarOff,
+                  "the merge buffer reuses the K/V ring, the query rows and the partial dots");
     constexpr int kQuarter = D / 4;               // columns per warp in phase A
     constexpr int kHalf = kQuarter / 2;           // columns per lane in phase A (16 or 8)
     static_assert(kKeys == 16, "phase A maps a warp's lanes to 16 keys x 2 column halves");
-    constexpr int kChunks = D * 2 / 16;           // 16-byte chunks per K/V row
     constexpr int kRowsA2 = (RPC + 3) / 4;        // rows per warp in phase A2
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
     float *qs = reinterpret_cast<float *>(smem + L::kQOff);
     float *part = reinterpret_cast<float *>(smem + L::kPartOff);
     float *ps = reinterpret_cast<float *>(smem + L::kPOff);
@@ -117,29 +128,28 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
     // CTA row r is group row r0 + r: query head kvh * rep + (r0 + r) / Nq, new row (r0 + r) % Nq,
     // i.e. global row ((b * H + h) * Nq + i) = kvh * rows + r0 + r
     const long grow0 = static_cast<long>(kvh) * p.rows + r0;
-    const T *kbase = reinterpret_cast<const T *>(p.k) + static_cast<size_t>(kvh) * p.Nk * D;
-    const T *vbase = reinterpret_cast<const T *>(p.v) + static_cast<size_t>(kvh) * p.Nk * D;
-
-    auto load_tile = [&](int t) {  // always commits a group, empty past the last tile
-        if (t < ntiles) {
-            const int key0 = k_begin + kKeys * t;
-            const int stage = t % kStages;
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kStages; ++s2) mbar_init(&full[s2], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    __syncthreads();
+    // Thread 0 fills stage t % kStages with the K and V boxes of tile t (keys past the cache's
+    // capacity read as zeros; keys past the range or the sequence length are masked in A2).
+    auto load_tile = [&](int t) {
+        if (tid != 0 || t >= ntiles) return;
+        const int key0 = k_begin + kKeys * t;
+        const int stage = t % kStages;
+        mbar_arrive_expect_tx(&full[stage], 2 * L::kTileBytes);
 #pragma unroll
-            for (int i = tid; i < 2 * kKeys * kChunks; i += kThreads) {
-                const int kv = i / (kKeys * kChunks);
-                const int rem = i - kv * kKeys * kChunks;
-                const int row = rem / kChunks, ch = rem - row * kChunks;
-                const int key = key0 + row;
-                const bool in = key < k_end;
-                const T *src =
-                    (kv ? vbase : kbase) + static_cast<size_t>(in ? key : 0) * D + ch * 8;
-                uint8_t *dst = kv ? smem + L::kVOff + stage * L::kVTileBytes + row * L::kVRowBytes
-                                  : smem + L::kKOff + stage * L::kKTileBytes + row * L::kKRowBytes;
-                dst += ch * 16;
-                cp_async_16(dst, src, in);
-            }
+        for (int b = 0; b < D / 64; ++b) {
+            tma_load_3d(smem + L::kKOff + stage * L::kTileBytes + b * L::kBoxBytes, &tmk, b * 64,
+                        key0, kvh, &full[stage]);
+            tma_load_3d(smem + L::kVOff + stage * L::kTileBytes + b * L::kBoxBytes, &tmv, b * 64,
+                        key0, kvh, &full[stage]);
         }
-        cp_async_commit();
     };
 #pragma unroll
     for (int t = 0; t < kStages - 1; ++t) load_tile(t);
@@ -162,21 +172,25 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
 #pragma unroll
     for (int r = 0; r < RPC; ++r) acc[r] = make_float2(0.f, 0.f);
 
-    for (int t = 0; t < ntiles; ++t) {
+    int t = 0;
+    for (; t < ntiles; ++t) {
         const int stage = t % kStages;
-        cp_async_wait_group<kStages - 2>();  // tile t has landed (this thread's part)
-        __syncthreads();  // ... everyone's part; and everyone is done with tile t - 1
-        load_tile(t + kStages - 1);  // into the stage tile t - 1 used
+        // tile t has landed; every thread is done with tile t - 1, whose stage is refilled
+        if (!mbar_wait(&full[stage], (t / kStages) & 1, p.ctl, abort_flag)) *abort_flag = 1;
+        __syncthreads();
+        if (*abort_flag) break;  // a wait ran out: every thread leaves the loop here
+        load_tile(t + kStages - 1);
 
         {  // A: partial dots of key `kl` over columns [c0, c0 + D/8), c0 = warp * D/4 + half * D/8
-            const uint8_t *krow = smem + L::kKOff + stage * L::kKTileBytes + kl * L::kKRowBytes +
-                                  (warp * kQuarter + half * kHalf) * 2;
+            const uint8_t *ktile = smem + L::kKOff + stage * L::kTileBytes;
+            const int c0 = warp * kQuarter + half * kHalf;
             float2 dot[RPC];  // even and odd columns summed apart (paired fp32 FMAs)
 #pragma unroll
             for (int r = 0; r < RPC; ++r) dot[r] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c8 = 0; c8 < kHalf / 8; ++c8) {
-                const uint4 kw = *reinterpret_cast<const uint4 *>(krow + c8 * 16);
+                const uint4 kw =
+                    *reinterpret_cast<const uint4 *>(ktile + swz_chunk(kl, (c0 >> 3) + c8));
                 const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y),
                              k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
 #pragma unroll
@@ -228,8 +242,7 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
         }
         __syncthreads();
         {  // B: O_g = alpha O_g + P V over this thread's key group, two columns, every row
-            const uint8_t *vcol = smem + L::kVOff + stage * L::kVTileBytes +
-                                  rs * kKeysB * L::kVRowBytes + cp * 4;
+            const uint8_t *vtile = smem + L::kVOff + stage * L::kTileBytes;
             const float *pg = ps + rs * kKeysB;
 #pragma unroll
             for (int r = 0; r < RPC; ++r) {
@@ -242,9 +255,11 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
             for (int k4 = 0; k4 < kKeysB; k4 += 4) {
                 float2 vv[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    vv[u] = unpack2<BF16>(
-                        *reinterpret_cast<const uint32_t *>(vcol + (k4 + u) * L::kVRowBytes));
+                for (int u = 0; u < 4; ++u) {
+                    const int key = rs * kKeysB + k4 + u;  // row of the tile
+                    vv[u] = unpack2<BF16>(*reinterpret_cast<const uint32_t *>(
+                        vtile + swz_chunk(key, cp >> 2) + (cp & 3) * 4));
+                }
 #pragma unroll
                 for (int r = 0; r < RPC; ++r) {
                     if (r < nrows) {  // rows past nrows have no probabilities this tile
@@ -260,7 +275,14 @@ __global__ void __launch_bounds__(kThreads) fa_decode_kernel(const DecodeParams 
             }
         }
     }
-    cp_async_wait_group<0>();  // no copy may still target shared memory at exit
+    if (*abort_flag) {
+        // let the copies still in flight land before shared memory is reused or released
+        if (tid == 0)
+            for (int u = t; u < min(ntiles, t + kStages - 1); ++u)
+                drain_wait(&full[u % kStages], (u / kStages) & 1, p.ctl);
+        __syncthreads();
+        return;
+    }
 
 #pragma unroll
     for (int i = 0; i < kRowsA2; ++i) {
@@ -394,26 +416,26 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
 }
 
 template <int D, bool BF16, int RPC>
-cudaError_t launch_decode_rpc(const DecodeParams &p, cudaStream_t stream) {
+cudaError_t launch_decode_rpc(const DecodeMaps &m, const DecodeParams &p, cudaStream_t stream) {
     using L = DecLayout<D, RPC>;
     auto kern = fa_decode_kernel<D, BF16, RPC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kBytes);
+                                         L::kAlloc);
     if (e != cudaSuccess) return e;
     const long grid = static_cast<long>(p.B) * p.Hkv * p.splits * p.row_groups;
-    kern<<<static_cast<unsigned>(grid), kThreads, L::kBytes, stream>>>(p);
+    kern<<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(m.k, m.v, p);
     return cudaGetLastError();
 }
 
 template <int D, bool BF16>
-cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
+cudaError_t launch_decode_t(const DecodeMaps &m, const DecodeParams &p, cudaStream_t stream) {
     const int rpc = p.rows >= 16 ? 16 : p.rows;  // rows per CTA: the row group size
     cudaError_t e;
-    if (rpc <= 1) e = launch_decode_rpc<D, BF16, 1>(p, stream);
-    else if (rpc <= 2) e = launch_decode_rpc<D, BF16, 2>(p, stream);
-    else if (rpc <= 4) e = launch_decode_rpc<D, BF16, 4>(p, stream);
-    else if (rpc <= 8) e = launch_decode_rpc<D, BF16, 8>(p, stream);
-    else e = launch_decode_rpc<D, BF16, 16>(p, stream);
+    if (rpc <= 1) e = launch_decode_rpc<D, BF16, 1>(m, p, stream);
+    else if (rpc <= 2) e = launch_decode_rpc<D, BF16, 2>(m, p, stream);
+    else if (rpc <= 4) e = launch_decode_rpc<D, BF16, 4>(m, p, stream);
+    else if (rpc <= 8) e = launch_decode_rpc<D, BF16, 8>(m, p, stream);
+    else e = launch_decode_rpc<D, BF16, 16>(m, p, stream);
     if (e != cudaSuccess || p.splits == 1) return e;
     // programmatic stream serialization: the merge's CTAs (small: 128 threads, 2 KB) are
     // scheduled beside the range kernel's last CTAs instead of after its completion
@@ -431,10 +453,12 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_decode_t<64, true>(p, stream)
-                             : launch_decode_t<64, false>(p, stream);
-    return bf16 ? launch_decode_t<128, true>(p, stream) : launch_decode_t<128, false>(p, stream);
+cudaError_t launch_decode(const DecodeMaps &m, const DecodeParams &p, int d, bool bf16,
+                          cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_decode_t<64, true>(m, p, stream)
+                             : launch_decode_t<64, false>(m, p, stream);
+    return bf16 ? launch_decode_t<128, true>(m, p, stream)
+                : launch_decode_t<128, false>(m, p, stream);
 }
 
 }  // namespace fa

@@ -149,6 +149,11 @@ struct DecodeParams {
     int splits, chunk;        // key ranges [s * chunk, (s + 1) * chunk), chunk a multiple of 32
     float scale_log2;         // scale * log2(e)
     int causal;               // new rows end-aligned with the cache
+    Ctl ctl;
+};
+
+struct DecodeMaps {
+    CUtensorMap k, v;         // [B*H_kv, Nk, d] cache, boxes 64 elements x 16 keys
 };
 
 struct Maps {
@@ -164,7 +169,8 @@ cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf
                             bool after_dq, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
                           cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams &p, int d, bool bf16, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeMaps &maps, const DecodeParams &p, int d, bool bf16,
+                          cudaStream_t stream);
 cudaError_t launch_fp8_transpose_v(const uint8_t *v, uint8_t *vt, int BHkv, int N, int Np, int d,
                                    cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const Fp8Maps &maps, const Fp8FwdParams &p, int d,
