@@ -124,6 +124,12 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
 // MMA order, one query tile of lookahead: dV(n), S^T(n+1), dK(n), dP^T(n+1), dV(n+1), ...
 // So the exponentials of tile n+1 overlap dK(n) and dP^T(n+1), and dS(n+1) overlaps dV(n+1)
 // and S^T(n+2).  One issuing thread keeps this order exact on the tensor pipe.
+// Head dimension 64: dV and dK take 128 columns, so a second S^T buffer fits at [384, 512)
+// (tile n uses buffer n % 2) and S^T(n+1) is issued before dV(n), which still reads P^T(n) from
+// the other buffer: S^T(n+1), dV(n), dK(n), dP^T(n+1).  The compute warps then find the next
+// tile's scores ready when they finish dS(n) (at d = 64 a tile's four GEMMs take half the tensor
+// time of d = 128 against the same element-wise work, and with one buffer the MMA warp waited
+// about 750 cycles per tile for the probabilities).
 // Grouped-query attention (FlashAttention-2 reading notes, MQA/GQA section): the query tiles
 // of every query head that shares this K/V head stream through the same pipeline, one head
 // after the other, so dK and dV are summed over the group in TMEM.  When there are too few K/V
@@ -140,9 +146,10 @@ struct DkvLayout {
     static constexpr int kSlotOff = 2 * kTileBytes;
     static constexpr int kLdOff = kSlotOff + kSlots * kTileBytes;  // 2 x (128 L + 128 D floats)
     static constexpr int kBarOff = kLdOff + 2 * 1024;
-    // kv_full, full[S], empty[S], ld_full[2], ld_empty[2], s_full, dp_full, p_ready, ds_ready,
-    // final, drain
-    static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 6;
+    // kv_full, full[S], empty[S], ld_full[2], ld_empty[2], s_full[2], dp_full, p_ready,
+    // ds_ready, final, drain
+    static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 7;
+    static constexpr bool kDbl = D == 64;  // two S^T buffers (see the kernel comment)
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kMaskOff = kMiscOff + 16;  // block-mask bits of the CTA's column / row
     static constexpr int kAlloc = kMaskOff + kMaskSmemWords * 4;  // 1024-aligned base (checked)
@@ -172,8 +179,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     uint64_t *empty = full + L::kSlots;
     uint64_t *ld_full = empty + L::kSlots;  // [2]
     uint64_t *ld_empty = ld_full + 2;       // [2]
-    uint64_t *s_full = ld_empty + 2;
-    uint64_t *dp_full = s_full + 1;
+    uint64_t *s_full = ld_empty + 2;        // [2]: one per S^T buffer (d = 64), else [0] only
+    uint64_t *dp_full = s_full + 2;
     uint64_t *p_ready = dp_full + 1;
     uint64_t *ds_ready = p_ready + 1;
     uint64_t *fin = ds_ready + 1;
@@ -201,7 +208,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             mbar_init(&ld_full[e], 32);   // one cp.async completion per lane of the load warp
             mbar_init(&ld_empty[e], kComputeWarps);  // every compute warp, after its dS
         }
-        mbar_init(s_full, 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
         mbar_init(dp_full, 1);
         mbar_init(p_ready, kComputeWarps);
         mbar_init(ds_ready, kComputeWarps);
@@ -292,7 +300,10 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         // the whole warp runs this loop in lockstep; one elected lane issues each MMA/commit
         {
             const uint32_t sSlot = smem_u32(smem + L::kSlotOff);
-            const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+            const uint32_t tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+            // S^T buffer of query tile n, and the barrier that says it holds S^T(n)
+            auto tS_of = [&](int n) { return tmem + ((L::kDbl && (n & 1)) ? 384u : 0u); };
+            auto sbar_of = [&](int n) { return &s_full[L::kDbl ? (n & 1) : 0]; };
             const SDesc dK0 = sdesc_make(smem_u32(smem + L::kKOff), 16, 1024);
             const SDesc dV0 = sdesc_make(smem_u32(smem + L::kVOff), 16, 1024);
             const SDesc dSk = sdesc_make(sSlot, 16, 1024);            // slot as K-major B
@@ -323,8 +334,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             if (ok && hq < hq_end) {
                 ok = full_wait(0) && full_wait(1);
                 if (ok) {
-                    issue_ss(tS, dK0, 0);
-                    umma_commit_el(s_full);
+                    issue_ss(tS_of(0), dK0, 0);
+                    umma_commit_el(sbar_of(0));
                     issue_ss(tdP, dV0, 1);
                     umma_commit_el(dp_full);
                     log_visit(hq, i);
@@ -335,21 +346,28 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 next_unit(p, mcol, kt, i0, hq_end, nhq, ni);
                 const bool more = nhq < hq_end;
                 const int lq = 2 * n, ldo = 2 * n + 1;  // this tile's Q and dO loads
+                auto issue_next_s = [&]() -> bool {  // S^T(n+1) = K Q^T
+                    if (!more) return true;
+                    if (!full_wait(lq + 2)) return false;
+                    issue_ss(tS_of(n + 1), dK0, lq + 2);
+                    umma_commit_el(sbar_of(n + 1));
+                    log_visit(nhq, ni);
+                    return true;
+                };
+                if (L::kDbl && !issue_next_s()) {  // into the other buffer, ahead of dV(n)
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait_warp(p_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                issue_ts(tdV, tS, ldo, n > 0);  // dV += P^T dO
+                issue_ts(tdV, tS_of(n), ldo, n > 0);  // dV += P^T dO
                 umma_commit_el(&empty[slot_of(ldo)]);
-                if (more) {
-                    if (!full_wait(lq + 2)) {
-                        ok = false;
-                        break;
-                    }
-                    issue_ss(tS, dK0, lq + 2);  // S^T(n+1) = K Q^T
-                    umma_commit_el(s_full);
-                    log_visit(nhq, ni);
+                if (!L::kDbl && !issue_next_s()) {  // over P^T(n), after dV(n) has read it
+                    ok = false;
+                    break;
                 }
                 if (!mbar_wait_warp(ds_ready, n & 1, p.ctl, abort_flag)) {
                     ok = false;
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         const int row = quad * 32 + lane;  // key row within the tile
         const int k_row = kt * kTile + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + kGroupCols * g, tdP = tS + 128;
+        const uint32_t tS0 = tmem + lane_base + kGroupCols * g, tdP = tS0 + 128;
         const float sl2 = p.scale_log2;
         int n = 0;
         bool ok = true;
@@ -405,8 +423,12 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     if (lane == r) keep = col;
                 }
             }
+            // S^T of this tile: buffer n % 2 at d = 64, the only one otherwise
+            const uint32_t tS = tS0 + ((L::kDbl && (n & 1)) ? 384u : 0u);
+            uint64_t *const sbar = &s_full[L::kDbl ? (n & 1) : 0];
+            const uint32_t spar = L::kDbl ? ((n >> 1) & 1) : (n & 1);
             if (!mbar_wait_warp(&ld_full[e], (n >> 1) & 1, p.ctl, abort_flag) ||
-                !mbar_wait_warp(s_full, n & 1, p.ctl, abort_flag)) {
+                !mbar_wait_warp(sbar, spar, p.ctl, abort_flag)) {
                 ok = false;
                 break;
             }
