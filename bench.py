@@ -48,7 +48,7 @@ L2_BYTES = 129e6  # GB300 L2 (129 MB)
 _CSRC = "exact_attention_staged_gb300/csrc/"
 _SHARED = (_CSRC + "sm100.cuh", _CSRC + "fa_internal.h")
 # Files whose content decides each kernel's code: a stored ncu traffic figure is used only
-# while their combined hash still matches the one recorded with it.
+# while their combined hash (comments left out) still matches the one recorded with it.
 KERNEL_SOURCES = {
     "fa_fwd_kernel": (_CSRC + "fa_fwd.cu",) + _SHARED,
     "fa_bwd_dkdv_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
@@ -105,11 +105,38 @@ def measured_peaks():
                 "source": "fallback"}
 
 
+def strip_comments(src):
+    """C/C++ source with its comments removed and each line's trailing blanks and the blank
+    lines dropped: what the compiler sees, so that editing a comment does not count as
+    changing the kernel.  String and character literals are kept whole."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c and src[j] != "\n":
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def source_hash(rels):
     h = hashlib.sha256()
     for rel in rels:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -925,7 +952,8 @@ def run_sweep(args):
     head dimension 64 and 128, without and with the causal mask.  bf16 inputs drawn on the
     device (iid N(0, 1), seeded); every call's inputs (201 MB or more) exceed the L2.  One JSON
     line per shape: forward, backward (D pre-pass, dK/dV, dQ) and forward+backward TFLOP/s over
-    --steps calls after --warmup, CUDA events on the launching stream."""
+    regions of --steps calls after --warmup, repeated until --min-region-s of each pass is
+    timed (CUDA events on the launching stream), with the SM clocks sampled in those regions."""
     from exact_attention_staged_gb300 import api
     api.load()
     dev = torch.device("cuda", 0)
@@ -933,17 +961,25 @@ def run_sweep(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(2048)
 
-    def per_call_ms(fn):
+    def per_call_ms(fn, clk):
+        """Mean per-call time over regions of --steps calls, repeated back to back until
+        --min-region-s of work is timed (at most 200 regions)."""
         for _ in range(args.warmup):
             fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(args.steps):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / args.steps
+        total_ms, calls = 0.0, 0
+        while True:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with clk.region():
+                a.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+            total_ms += a.elapsed_time(b)
+            calls += args.steps
+            if total_ms >= 1e3 * args.min_region_s or calls >= 200 * args.steps:
+                return total_ms / calls
 
     for d in (64, 128):
         for causal in (False, True):
@@ -965,8 +1001,9 @@ def run_sweep(args):
                             workspace=ws)
 
                 fwd()
-                t_f = per_call_ms(fwd)
-                t_b = per_call_ms(bwd)
+                with ClockSampler(dev.index) as clk:
+                    t_f = per_call_ms(fwd, clk)
+                    t_b = per_call_ms(bwd, clk)
                 status = api.sync_status()
                 f = flops(B, H, N, d, causal)["fa_fwd_kernel"]
                 print(json.dumps({
@@ -974,7 +1011,8 @@ def run_sweep(args):
                     "d": d, "causal": causal, "dtype": "bf16", "status": status,
                     "fwd_ms": t_f, "bwd_ms": t_b,
                     "fwd_tflops": f / t_f / 1e9, "bwd_tflops": 2.5 * f / t_b / 1e9,
-                    "fwd_bwd_tflops": 3.5 * f / (t_f + t_b) / 1e9}), flush=True)
+                    "fwd_bwd_tflops": 3.5 * f / (t_f + t_b) / 1e9,
+                    "clocks": clk.summary()}), flush=True)
                 del q, k, v, do, o, lse, dq, dk, dv, ws
     return 0
 

@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kKeys = 16;     // keys per shared-memory tile (lane = key and column half)
-constexpr int kStages = 3;    // K/V tiles in the cp.async ring (two in flight while one is used)
+constexpr int kStages = 3;    // K/V tiles in the TMA ring (two in flight while one is used)
 
 template <int D, int RPC>
 struct DecLayout {

@@ -123,6 +123,19 @@ def test_stored_traffic_is_used_only_while_the_kernel_sources_match(monkeypatch)
     assert bench.decode_traffic("decode_gqa_d128_kv8k", 1) is None
 
 
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = 'int f(int x) {  // doubles\n  /* "quoted" */ return 2 * x; }\nconst char *s = "a // b";\n'
+    (tmp_path / "a.cu").write_text(src)
+    (tmp_path / "b.cu").write_text("// header comment\n\n" + src.replace("// doubles", "// twice"))
+    (tmp_path / "c.cu").write_text(src.replace("2 * x", "3 * x"))
+    (tmp_path / "d.cu").write_text(src.replace('"a // b"', '"a // c"'))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = {n: bench.source_hash((n,)) for n in ("a.cu", "b.cu", "c.cu", "d.cu")}
+    assert h["a.cu"] == h["b.cu"]        # comments and blank lines only
+    assert h["a.cu"] != h["c.cu"]        # code
+    assert h["a.cu"] != h["d.cu"]        # a string literal that holds comment markers
+
+
 def test_clock_summary_keeps_only_samples_inside_the_timed_regions():
     clk = bench.ClockSampler(0)
     line = "{},2070,Not Active,Not Active,Not Active,{}"
