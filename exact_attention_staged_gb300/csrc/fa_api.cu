@@ -218,10 +218,11 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     if (rc != FA_OK) return rc;
     fa::Maps maps;
     const int BH = B * H;
+    // the forward stores O row by row from registers: no output map
     if (make_map(&maps.q, q, BH, N, d, dtype) || make_map(&maps.k, k, B * Hkv, N, d, dtype) ||
-        make_map(&maps.v, v, B * Hkv, N, d, dtype) || make_map(&maps.out0, o, BH, N, d, dtype))
+        make_map(&maps.v, v, B * Hkv, N, d, dtype))
         return FA_ERR_CUDA;
-    maps.out1 = maps.out0;
+    maps.out0 = maps.out1 = maps.q;
     fa::FwdParams p;
     p.o = o;
     p.lse = lse;

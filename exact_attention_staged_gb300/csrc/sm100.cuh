@@ -565,6 +565,34 @@ __device__ __forceinline__ void griddep_wait() {
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Cluster launch control (PTX clusterlaunchcontrol, sm_100 and later).  try_cancel asks the
+// hardware to cancel one CTA of this grid that has not started yet; the 16-byte answer lands in
+// shared memory (16-byte aligned) and completes 16 transaction bytes on `bar`, whose expected
+// count the caller has raised.  A CTA that wins a cancelled CTA's index does that CTA's work,
+// so a grid of one CTA per work unit runs as a persistent grid that the hardware keeps fed in
+// launch order.  After a failed answer (nothing left to cancel) no further request is made.
+__device__ __forceinline__ void clc_try_cancel(void *resp16, uint64_t *bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+        " [%0], [%1];" ::"r"(smem_u32(resp16)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+// x index of the CTA an answer cancelled, or -1 when it cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(const void *resp16) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(smem_u32(resp16))
+        : "memory");
+    return ok ? static_cast<int>(x) : -1;
+}
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {

@@ -107,10 +107,11 @@ def test_block_sparse_small(cuda_lib, N, d, causal, seed):
     assert torch.all(grads[0][:, :, 128:256].cpu() == 0)
 
 
-@pytest.mark.parametrize("T", [4096, 4097])
+@pytest.mark.parametrize("T", [2048, 2049, 4096, 4097])
 def test_block_mask_wider_than_shared_copy(cuda_lib, T):
-    # The kernels copy a mask row or column of up to 4096 tiles into shared memory as bits and
-    # read wider masks from global memory.  A mask of 2 x 2 diagonal super-blocks (and a lone
+    # The forward copies the mask rows of its query tiles into shared memory as bits when the
+    # mask is at most 2048 tiles wide, the backward kernels a row or column of up to 4096 tiles;
+    # wider masks are read from global memory.  A mask of 2 x 2 diagonal super-blocks (and a lone
     # last block when T is odd) splits the attention into independent problems of 256 rows
     # (keys and queries alike), which the oracle solves one at a time.
     N, d = T * BLOCK, 64
