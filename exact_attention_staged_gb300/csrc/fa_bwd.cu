@@ -146,9 +146,9 @@ struct DkvLayout {
     static constexpr int kSlotOff = 2 * kTileBytes;
     static constexpr int kLdOff = kSlotOff + kSlots * kTileBytes;  // 2 x (128 L + 128 D floats)
     static constexpr int kBarOff = kLdOff + 2 * 1024;
-    // kv_full, full[S], empty[S], ld_full[2], ld_empty[2], s_full[2], dp_full, p_ready,
+    // kv_full, full[S], empty[S], ld_full[2], ld_empty[2], s_full[2], dp_full, p_ready[2],
     // ds_ready, final, drain
-    static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 7;
+    static constexpr int kNumBars = 1 + 2 * kSlots + 4 + 8;
     static constexpr bool kDbl = D == 64;  // two S^T buffers (see the kernel comment)
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kMaskOff = kMiscOff + 16;  // block-mask bits of the CTA's column / row
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
     uint64_t *ld_empty = ld_full + 2;       // [2]
     uint64_t *s_full = ld_empty + 2;        // [2]: one per S^T buffer (d = 64), else [0] only
     uint64_t *dp_full = s_full + 2;
-    uint64_t *p_ready = dp_full + 1;
-    uint64_t *ds_ready = p_ready + 1;
+    uint64_t *p_ready = dp_full + 1;        // [2]: one per S^T buffer (d = 64), else [0] only
+    uint64_t *ds_ready = p_ready + 2;
     uint64_t *fin = ds_ready + 1;
     uint64_t *drain = fin + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_ready, kComputeWarps);
+        mbar_init(&p_ready[0], kComputeWarps);
+        mbar_init(&p_ready[1], kComputeWarps);
         mbar_init(ds_ready, kComputeWarps);
         mbar_init(fin, 1);
         mbar_init(drain, 1);
@@ -358,7 +359,10 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     ok = false;
                     break;
                 }
-                if (!mbar_wait_warp(p_ready, n & 1, p.ctl, abort_flag)) {
+                // at d = 64 a compute warp may post P^T(n+1) (its S^T was issued ahead of dV(n))
+                // before a slower warp has posted P^T(n): each S^T buffer has its own barrier
+                if (!mbar_wait_warp(&p_ready[L::kDbl ? (n & 1) : 0],
+                                    L::kDbl ? ((n >> 1) & 1) : (n & 1), p.ctl, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             } else {
                 tmem_st16(tS, pk);
             }
-            mbar_arrive_warp_after_st(p_ready);
+            mbar_arrive_warp_after_st(&p_ready[L::kDbl ? (n & 1) : 0]);
             if (!mbar_wait_warp(dp_full, n & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;

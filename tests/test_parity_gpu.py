@@ -188,6 +188,29 @@ def test_deterministic(cuda_lib):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("d, causal", [(64, False), (64, True), (128, False)])
+def test_dkdv_repeatable_over_long_key_walks(cuda_lib, d, causal):
+    # dK/dV at head dimension 64 issues the next S^T before dV of the current query tile, so its
+    # compute warps can drift a tile apart; each S^T buffer has its own probability-ready
+    # barrier for that reason.  Long key walks (128 query tiles a key tile) and many CTAs per
+    # SM give the drift room: dK and dV must come out bit for bit the same every call.
+    t = make_inputs(1, 8, 16384, d, torch.bfloat16, seed=37)
+    q, k, v, do = (t[x].to(DEV) for x in ("q", "k", "v", "do"))
+    o, lse = cuda_lib.fwd(q, k, v, d ** -0.5, causal=causal)
+    delta = torch.empty_like(lse)
+    cuda_lib.bwd_preprocess(o, do, delta)
+    first = None
+    for _ in range(4):
+        dk, dv = cuda_lib.bwd_dkdv(q, k, v, do, lse, delta, torch.empty_like(q),
+                                   torch.empty_like(q), d ** -0.5, causal)
+        assert cuda_lib.sync_status() == 0
+        assert bool(torch.isfinite(dv).all()) and bool(torch.isfinite(dk).all())
+        if first is None:
+            first = (dk.clone(), dv.clone())
+        else:
+            assert torch.equal(first[0], dk) and torch.equal(first[1], dv)
+
+
 def test_backward_stages_match_fused_call(cuda_lib):
     t = make_inputs(1, 2, 500, 64, torch.bfloat16, seed=41)
     q, k, v, do = (t[x].to(DEV) for x in ("q", "k", "v", "do"))
