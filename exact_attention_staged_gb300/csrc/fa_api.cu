@@ -404,27 +404,24 @@ int bwd_entry(const void *q, const void *k, const void *v, const void *o, const 
                    scale, causal, block_mask, drop, stream);
 }
 
-// Decode key ranges: as many per (K/V head, row group) as give about 28 128-thread CTAs per SM
-// of a 152-SM GB300 (four waves of seven resident CTAs), but no range shorter than 256 keys;
-// ranges are multiples of 32 keys (two of the kernel's 16-key tiles).  A CTA works through its
-// tiles with block-wide barriers, so more resident CTAs, not a deeper prefetch ring, keep the
-// memory system busy (measured on the 8k-cache workload: 3 CTAs per SM of the earlier 32-key
-// kernel reached 0.49 of the copy bandwidth, 12 reached 0.57, a 5-stage ring was slower; the
-// 16-key kernel at 7, 14, 21 and 28 CTAs per SM: 0.120, 0.119, 0.120 and 0.117 ms per step).
-constexpr long kDecodeWaveCtas = 28 * 152;
+// Key ranges of decode: a unit is (K/V head, key range, group of up to 128 query rows) and the
+// grid runs one CTA per SM that walks the units, so the ranges are cut to give each SM about
+// eight units (the last ones then finish within about an eighth of a unit of each other) but
+// never shorter than four 128-key tiles.
+constexpr long kDecodeUnitsTarget = 8 * 152;
 struct DecodeSplit {
     int splits, chunk, row_groups;
 };
 DecodeSplit decode_split(int B, int H, int Hkv, int Nq, int Nk) {
     const int rows = (H / Hkv) * Nq;
-    const int row_groups = (rows + 15) / 16;
+    const int row_groups = (rows + 127) / 128;
     const long units = static_cast<long>(B) * Hkv * row_groups;
-    long s = kDecodeWaveCtas / units;
-    const long max_s = (Nk + 255) / 256;
+    long s = (kDecodeUnitsTarget + units - 1) / units;
+    const long max_s = (Nk + 511) / 512;
     if (s > max_s) s = max_s;
     if (s < 1) s = 1;
     int chunk = static_cast<int>((Nk + s - 1) / s);
-    chunk = (chunk + 31) / 32 * 32;
+    chunk = (chunk + 127) / 128 * 128;
     return {(Nk + chunk - 1) / chunk, chunk, row_groups};
 }
 
@@ -667,8 +664,8 @@ int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
     p.causal = causal ? 1 : 0;
     if (make_ctl(status, 0, 0, &p.ctl) != FA_OK) return FA_ERR_INVALID;
     fa::DecodeMaps maps;
-    if (make_map(&maps.k, k, B * H_kv, Nk, d, dtype, 16) ||
-        make_map(&maps.v, v, B * H_kv, Nk, d, dtype, 16))
+    if (make_map(&maps.q, q, 1, B * H * Nq, d, dtype) || make_map(&maps.k, k, B * H_kv, Nk, d, dtype) ||
+        make_map(&maps.v, v, B * H_kv, Nk, d, dtype))
         return FA_ERR_CUDA;
     cudaError_t e = fa::launch_decode(maps, p, d, dtype == FA_BF16,
                                       static_cast<cudaStream_t>(stream));

@@ -1,35 +1,28 @@
 // fa_decode.cu - decode: a few new query rows per sequence against a KV cache, sm_103a.
 //
 // FlashAttention-2 reading notes, section on the KV cache: in the decode phase each step's
-// query is 1 x d (a few rows here) against the N cached keys, so the product is a matrix-vector
-// one and the kernel is bound by reading K and V from HBM, not by arithmetic.  The work is
-// therefore split over the cache, not over queries: CTA (K/V head, key range, row group) runs
-// the online softmax (running max m and sum l per row, FlashAttention-2 Algorithm 1) over its
-// key range for every query row that reads this K/V head (all query heads of a grouped-query
-// group, times the new rows), reading each cached K/V row once.  Key ranges are merged by the
-// statistic merge of the FlashAttention paper detail, Technique 1 (m = max(m1, m2),
-// l = e^(m1-m) l1 + e^(m2-m) l2, and the outputs weighted the same way).
+// query is a few rows against the N cached keys, so the work is bound by reading K and V from
+// HBM, not by arithmetic, and it is split over the cache: a work unit is (K/V head, key range,
+// group of up to 128 query rows) and runs the online softmax (running max m and sum l per row,
+// FlashAttention-2 Algorithm 1) over its key range for every query row that reads this K/V head
+// (all query heads of a grouped-query group, times the new rows), reading each cached K/V row
+// once.  Key ranges are merged by the statistic merge of the FlashAttention paper detail,
+// Technique 1 (m = max(m1, m2), l = e^(m1-m) l1 + e^(m2-m) l2, and the outputs weighted the same
+// way), in range order.
 //
-// GB300 mapping: no tensor cores (one to sixteen rows per key: 4 to 64 FLOP per 16-bit K/V
-// element pair, far below what would make the MMA pipe the limit); 128 threads per CTA, seven
-// CTAs per SM at up to four rows (each CTA's tile loop is a chain of barriers and shuffles, so
-// resident CTAs set the rate).  K and V tiles of 16 keys stream through a three-stage ring
-// filled by TMA (one thread issues a tile's boxes; completion on the stage's mbarrier), in boxes
-// of 64 elements x 16 keys with the 128-byte swizzle: 16-byte chunk c of key row r sits at
-// chunk position c ^ (r mod 8), so the 16-byte reads of 8 consecutive key rows (phase A) and the
-// 128-byte row reads (phase B) are free of bank conflicts without padding.  Per tile:
-//   A   every warp takes a quarter of d, every lane one key and half of that quarter: partial
-//       dot products of that key with all rows (query rows broadcast from shared memory, fp32,
-//       pre-scaled by scale * log2 e), the two halves summed by one shuffle;
-//   A2  warp w owns rows w, w+4, ...: sums the four quarters, masks, takes the tile max with
-//       shuffles over 16 lanes, P = 2^(s - m), l = alpha l + sum P;
-//   B   every thread owns two output columns of every row and a fixed share of the tile's keys
-//       (key group): O_g = alpha O_g + P V over its keys, P read four keys per shared load, so
-//       each V element and each probability is read from shared memory once per tile.
-// The key groups' partial outputs share the row statistics (alpha is per row and tile), so they
-// are summed once, after the last tile.  With one key range the CTA then writes O and LSE;
-// otherwise it writes (m, l, unnormalised O) and fa_decode_combine_kernel merges the ranges in
-// order (deterministic).
+// GB300 mapping: the products run on the tensor cores even though a unit has only a handful of
+// real query rows, so that the SM's own pipes are left with the softmax alone and the kernel can
+// stream K and V at the HBM rate: the unit's query rows are the first rows of a 128-row A tile
+// (a group's rows are consecutive rows of Q, loaded by TMA; the tile's other rows belong to the
+// next groups or read as zeros, and their results are never stored), S = Q K_j^T is a 128 x 128
+// tcgen05 MMA into tensor memory, one softmax thread per row (as in the forward) turns it into
+// P~ = 2^(S scale log2 e - m) over S, and O += P~ V_j takes P~ from tensor memory.  Per CTA
+// (192 threads, one per SM): warp 0 loads (Q of each unit, K_j and V_j of 128 keys into a ring),
+// warp 1 issues the MMAs, warps 2..5 run the softmax of their 32-row quarter (only quarters
+// holding real rows do the arithmetic).  S has two buffers, so S_{j+1} is computed while the
+// softmax of S_j runs.  The grid has one CTA per unit, and the CTAs that start walk the units
+// of those that have not (cluster launch control, as in the forward), so the ring streams across
+// unit boundaries.
 #include "fa_internal.h"
 
 #include <cmath>
@@ -38,292 +31,453 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kKeys = 16;     // keys per shared-memory tile (lane = key and column half)
-constexpr int kStages = 3;    // K/V tiles in the TMA ring (two in flight while one is used)
+constexpr int kDecTile = 128;  // keys per K/V tile, rows per query tile (the MMA's M)
 
-template <int D, int RPC>
+template <int D>
 struct DecLayout {
-    static constexpr int kBoxBytes = kKeys * 128;                   // 64 elements x 16 keys
-    static constexpr int kTileBytes = kKeys * D * 2;                // D / 64 boxes
-    static constexpr int kKOff = 0;                                 // kStages tiles (1024-aligned)
-    static constexpr int kVOff = kKOff + kStages * kTileBytes;      // kStages tiles
-    static constexpr int kQOff = kVOff + kStages * kTileBytes;      // float [RPC][D]
-    static constexpr int kPartOff = kQOff + RPC * D * 4;            // float [4][RPC][kKeys]
-    static constexpr int kPOff = kPartOff + 4 * RPC * kKeys * 4;    // float [RPC][kKeys]
-    static constexpr int kStatOff = kPOff + RPC * kKeys * 4;        // alpha, m, l [RPC] each
-    static constexpr int kBarOff = (kStatOff + 3 * RPC * 4 + 7) / 8 * 8;  // full[kStages]
-    static constexpr int kAbortOff = kBarOff + kStages * 8;
-    static constexpr int kBytes = kAbortOff + 8;
-    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 bytes
+    static constexpr int kTileBytes = kDecTile * D * 2;   // one 128 x d tile of 16-bit values
+    static constexpr int kBoxes = D / 64;                 // 128-byte-wide TMA boxes per tile row
+    static constexpr int kBoxBytes = kDecTile * 128;      // 16 KB
+    static constexpr int kStages = (D == 128) ? 3 : 6;    // K/V tile pairs in the ring
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = kTileBytes;           // [stage][K, V]
+    static constexpr int kBarOff = kRingOff + kStages * 2 * kTileBytes;
+    // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, o_final,
+    // unit_full[2], unit_empty[2], sched, drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 12;
+    static constexpr int kSchedOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // 16-byte answer
+    static constexpr int kUnitOff = kSchedOff + 16;      // int unit[2]
+    static constexpr int kMiscOff = kUnitOff + 8;        // TMEM base, abort flag
+    static constexpr int kBytes = kMiscOff + 8;
+    static constexpr int kAlloc = kBytes + 1024;         // room to align the base to 1024 bytes
+    static constexpr int kThreads = 192;
+    static constexpr uint32_t kTmemCols = 512;           // S_0, S_1 (2 x 128) + O (d)
+    static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
-
-// Byte offset of the 16-byte chunk holding elements [8 c, 8 c + 8) of key row r in a tile of
-// 128-byte-swizzled 64-element boxes.
-__device__ __forceinline__ int swz_chunk(int r, int c) {
-    return (c >> 3) * (kKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
 
 template <bool BF16>
 using elem_t = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
-// reductions over each 16-lane half of a warp (both halves hold the same 16 keys)
-__device__ __forceinline__ float half_max(float v) {
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float half_sum(float v) {
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// RPC: query rows per CTA (1, 2, 4, 8 or 16), the smallest that holds a K/V head's rows.
-template <int D, bool BF16, int RPC>
-__global__ void __launch_bounds__(kThreads)
-    fa_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                     const DecodeParams p) {
-    using L = DecLayout<D, RPC>;
-    using T = elem_t<BF16>;
-    constexpr int kPairs = D / 2;                 // column pairs of O
-    constexpr int kRB = kThreads / kPairs;        // key groups in phase B (2 for d=128, 4 for 64)
-    constexpr int kKeysB = kKeys / kRB;           // keys per group and tile (16 or 8)
-    constexpr int kRowsB = (RPC + kRB - 1) / kRB; // rows per thread in the final merge and store
-    static_assert(kKeysB % 4 == 0, "probabilities are read four keys at a time");
-    static_assert(kRB * RPC * D * 4 <= L::kBarOff,
-                  "the merge buffer reuses the K/V ring, the query rows and the partial dots");
-    constexpr int kQuarter = D / 4;               // columns per warp in phase A
-    constexpr int kHalf = kQuarter / 2;           // columns per lane in phase A (16 or 8)
-    static_assert(kKeys == 16, "phase A maps a warp's lanes to 16 keys x 2 column halves");
-    constexpr int kRowsA2 = (RPC + 3) / 4;        // rows per warp in phase A2
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbortOff);
-    float *qs = reinterpret_cast<float *>(smem + L::kQOff);
-    float *part = reinterpret_cast<float *>(smem + L::kPartOff);
-    float *ps = reinterpret_cast<float *>(smem + L::kPOff);
-    float *alpha_s = reinterpret_cast<float *>(smem + L::kStatOff);
-    float *m_s = alpha_s + RPC;
-    float *l_s = m_s + RPC;
-
-    // block order: row group fastest, then key range, then K/V head (b * H_kv + g)
-    unsigned bid = blockIdx.x;
+// One work unit: a key range of one K/V head for one group of its query rows.
+struct DecUnit {
+    int kvh, split, r0, nrows;  // K/V head (b * H_kv + g); range; first group row; real rows
+    int len;                    // keys of the sequence (kv_len clamped to [0, Nk])
+    int k_begin, k_end, ntiles; // the range [k_begin, k_end) in 128-key tiles
+    long grow0;                 // global row of the group's first row
+};
+__device__ __forceinline__ DecUnit dec_unit(const DecodeParams &p, int unit) {
+    unsigned bid = static_cast<unsigned>(unit);  // row group fastest, then key range, then K/V head
+    DecUnit u;
     const int rg = static_cast<int>(bid % static_cast<unsigned>(p.row_groups));
     bid /= static_cast<unsigned>(p.row_groups);
-    const int split = static_cast<int>(bid % static_cast<unsigned>(p.splits));
-    const int kvh = static_cast<int>(bid / static_cast<unsigned>(p.splits));
-    const int b = kvh / p.Hkv;
-    const int r0 = rg * RPC;
-    const int nrows = min(RPC, p.rows - r0);
+    u.split = static_cast<int>(bid % static_cast<unsigned>(p.splits));
+    u.kvh = static_cast<int>(bid / static_cast<unsigned>(p.splits));
+    const int b = u.kvh / p.Hkv;
+    u.r0 = rg * kDecTile;
+    u.nrows = min(kDecTile, p.rows - u.r0);
     int len = p.kv_len != nullptr ? p.kv_len[b] : p.Nk;
-    len = max(0, min(len, p.Nk));
-    const int k_begin = split * p.chunk;
-    const int k_end = min(k_begin + p.chunk, len);
-    const int ntiles = k_end > k_begin ? (k_end - k_begin + kKeys - 1) / kKeys : 0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kl = lane & (kKeys - 1), half = lane >> 4;  // phase A / A2: key, column half
-    // CTA row r is group row r0 + r: query head kvh * rep + (r0 + r) / Nq, new row (r0 + r) % Nq,
-    // i.e. global row ((b * H + h) * Nq + i) = kvh * rows + r0 + r
-    const long grow0 = static_cast<long>(kvh) * p.rows + r0;
-    if (tid == 0) {
-        for (int s2 = 0; s2 < kStages; ++s2) mbar_init(&full[s2], 1);
+    u.len = max(0, min(len, p.Nk));
+    u.k_begin = u.split * p.chunk;
+    u.k_end = min(u.k_begin + p.chunk, u.len);
+    u.ntiles = u.k_end > u.k_begin ? (u.k_end - u.k_begin + kDecTile - 1) / kDecTile : 0;
+    // group row r is query head kvh * rep + (r0 + r) / Nq, new row (r0 + r) % Nq, i.e. global
+    // row ((b * H + h) * Nq + i) = kvh * rows + r0 + r
+    u.grow0 = static_cast<long>(u.kvh) * p.rows + u.r0;
+    return u;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+    using L = DecLayout<D>;
+    constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false);
+    constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, true);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *q_empty = bars + 1;
+    uint64_t *kv_full = bars + 2;
+    uint64_t *kv_empty = kv_full + L::kStages;
+    uint64_t *s_full = kv_empty + L::kStages;  // [2]: one per S buffer
+    uint64_t *p_full = s_full + 2;             // [2]: one per S buffer
+    uint64_t *pv_done = p_full + 2;
+    uint64_t *o_final = pv_done + 1;
+    uint64_t *unit_full = o_final + 1;         // [2]
+    uint64_t *unit_empty = unit_full + 2;      // [2]
+    uint64_t *sched = unit_empty + 2;
+    uint64_t *drain = sched + 1;
+    void *sched_answer = smem + L::kSchedOff;
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(smem + L::kUnitOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMiscOff + 4);
+    const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
+
+    const int warp = warp_id(), lane = lane_id();
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 4);   // the four softmax warps
+            mbar_init(&unit_full[b], 1);
+            mbar_init(&unit_empty[b], 5);  // the MMA warp and the four softmax warps
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(o_final, 1);
+        mbar_init(sched, 1);
+        mbar_init(drain, 1);
+        unit_slot[0] = static_cast<int>(blockIdx.x);  // the first unit is this CTA's own
         *abort_flag = 0;
         fence_barrier_init();
+        tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
-    // Thread 0 fills stage t % kStages with the K and V boxes of tile t (keys past the cache's
-    // capacity read as zeros; keys past the range or the sequence length are masked in A2).
-    auto load_tile = [&](int t) {
-        if (tid != 0 || t >= ntiles) return;
-        const int key0 = k_begin + kKeys * t;
-        const int stage = t % kStages;
-        mbar_arrive_expect_tx(&full[stage], 2 * L::kTileBytes);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b) {
-            tma_load_3d(smem + L::kKOff + stage * L::kTileBytes + b * L::kBoxBytes, &tmk, b * 64,
-                        key0, kvh, &full[stage]);
-            tma_load_3d(smem + L::kVOff + stage * L::kTileBytes + b * L::kBoxBytes, &tmv, b * 64,
-                        key0, kvh, &full[stage]);
-        }
-    };
-#pragma unroll
-    for (int t = 0; t < kStages - 1; ++t) load_tile(t);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     // the range merge queued after this grid may take its SM slots early (it waits for this
     // grid's completion before it reads a partial result)
-    if (tid == 0) griddep_launch_dependents();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
-    const T *qrows = reinterpret_cast<const T *>(p.q) + static_cast<size_t>(grow0) * D;
-    for (int i = tid; i < RPC * D; i += kThreads)
-        qs[i] = i < nrows * D ? static_cast<float>(qrows[i]) * p.scale_log2 : 0.f;
-
-    float m_run[kRowsA2], l_run[kRowsA2];
-#pragma unroll
-    for (int i = 0; i < kRowsA2; ++i) {
-        m_run[i] = -INFINITY;
-        l_run[i] = 0.f;
-    }
-    const int cp = tid % kPairs, rs = tid / kPairs;  // column pair; key group (phase B)
-    float2 acc[RPC];  // this thread's two output columns of every row, over its key group
-#pragma unroll
-    for (int r = 0; r < RPC; ++r) acc[r] = make_float2(0.f, 0.f);
-
-    int t = 0;
-    for (; t < ntiles; ++t) {
-        const int stage = t % kStages;
-        // tile t has landed; every thread is done with tile t - 1, whose stage is refilled
-        if (!mbar_wait(&full[stage], (t / kStages) & 1, p.ctl, abort_flag)) *abort_flag = 1;
-        __syncthreads();
-        if (*abort_flag) break;  // a wait ran out: every thread leaves the loop here
-        load_tile(t + kStages - 1);
-
-        {  // A: partial dots of key `kl` over columns [c0, c0 + D/8), c0 = warp * D/4 + half * D/8
-            const uint8_t *ktile = smem + L::kKOff + stage * L::kTileBytes;
-            const int c0 = warp * kQuarter + half * kHalf;
-            float2 dot[RPC];  // even and odd columns summed apart (paired fp32 FMAs)
-#pragma unroll
-            for (int r = 0; r < RPC; ++r) dot[r] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c8 = 0; c8 < kHalf / 8; ++c8) {
-                const uint4 kw =
-                    *reinterpret_cast<const uint4 *>(ktile + swz_chunk(kl, (c0 >> 3) + c8));
-                const float2 k0 = unpack2<BF16>(kw.x), k1 = unpack2<BF16>(kw.y),
-                             k2 = unpack2<BF16>(kw.z), k3 = unpack2<BF16>(kw.w);
-#pragma unroll
-                for (int r = 0; r < RPC; ++r) {  // rows past nrows hold zeros
-                    const float4 *qv =
-                        reinterpret_cast<const float4 *>(qs + r * D + warp * kQuarter +
-                                                         half * kHalf + c8 * 8);
-                    const float4 a = qv[0], c = qv[1];
-                    float2 d = dot[r];
-                    d = ffma2(make_float2(a.x, a.y), k0, d);
-                    d = ffma2(make_float2(a.z, a.w), k1, d);
-                    d = ffma2(make_float2(c.x, c.y), k2, d);
-                    d = ffma2(make_float2(c.z, c.w), k3, d);
-                    dot[r] = d;
+    if (warp == 0) {
+        // ---------------------------------------------------------------- load warp
+        // The whole warp walks the units; lane 0 issues the copies and requests.
+        if (lane == 0) mbar_arrive(&unit_full[0]);
+        int unit = static_cast<int>(blockIdx.x);
+        int n = 0;     // K/V tile pairs issued
+        int nq = 0;    // Q tiles issued
+        int nreq = 0;  // scheduler requests made
+        bool more = true;
+        bool ok = true;
+        for (int k = 0;; ++k) {
+            const DecUnit u = dec_unit(p, unit);
+            auto load_q = [&]() {  // the Q tile is free once the previous unit's last S is done
+                if (nq > 0 && !mbar_wait_warp(q_empty, (nq - 1) & 1, p.ctl, abort_flag))
+                    return false;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, L::kTileBytes);
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(smem + L::kQOff + b * L::kBoxBytes, &tmq, b * 64,
+                                    static_cast<int>(u.grow0), 0, q_full);
                 }
-            }
-#pragma unroll
-            for (int r = 0; r < RPC; ++r) {  // the two column halves of key kl summed
-                float sp = dot[r].x + dot[r].y;
-                sp += __shfl_xor_sync(0xffffffffu, sp, 16);
-                if (half == 0) part[(warp * RPC + r) * kKeys + kl] = sp;
-            }
-        }
-        __syncthreads();
-        {  // A2: warp w owns rows w, w + 4, w + 8, w + 12
-            const int key = k_begin + kKeys * t + kl;
-#pragma unroll
-            for (int i = 0; i < kRowsA2; ++i) {
-                const int r = warp + 4 * i;
-                if (r < nrows) {
-                    const int gr = r0 + r;
-                    const int last = p.causal ? len - p.Nq + gr % p.Nq : len - 1;
-                    float s = part[r * kKeys + kl] + part[(RPC + r) * kKeys + kl] +
-                              part[(2 * RPC + r) * kKeys + kl] +
-                              part[(3 * RPC + r) * kKeys + kl];
-                    if (key >= k_end || key > last) s = -INFINITY;
-                    const float m_new = fmaxf(m_run[i], half_max(s));
-                    float alpha = 1.f, pr = 0.f;
-                    if (m_new != -INFINITY) {  // ex2(-inf) = 0 covers masked keys, first tile
-                        alpha = ex2(m_run[i] - m_new);
-                        pr = ex2(s - m_new);
-                    }
-                    l_run[i] = l_run[i] * alpha + half_sum(pr);
-                    m_run[i] = m_new;
-                    if (half == 0) ps[r * kKeys + kl] = pr;
-                    if (lane == 0) alpha_s[r] = alpha;
+                ++nq;
+                return true;
+            };
+            bool q_done = false;
+            for (int t = 0; t < u.ntiles && ok; ++t) {
+                const int s = n % L::kStages;
+                if (!mbar_wait_warp(&kv_empty[s], ((n / L::kStages) & 1) ^ 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            }
-        }
-        __syncthreads();
-        {  // B: O_g = alpha O_g + P V over this thread's key group, two columns, every row
-            const uint8_t *vtile = smem + L::kVOff + stage * L::kTileBytes;
-            const float *pg = ps + rs * kKeysB;
-#pragma unroll
-            for (int r = 0; r < RPC; ++r) {
-                if (r < nrows) {
-                    const float a = alpha_s[r];
-                    acc[r] = fmul2(acc[r], make_float2(a, a));
-                }
-            }
-#pragma unroll
-            for (int k4 = 0; k4 < kKeysB; k4 += 4) {
-                float2 vv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int key = rs * kKeysB + k4 + u;  // row of the tile
-                    vv[u] = unpack2<BF16>(*reinterpret_cast<const uint32_t *>(
-                        vtile + swz_chunk(key, cp >> 2) + (cp & 3) * 4));
-                }
-#pragma unroll
-                for (int r = 0; r < RPC; ++r) {
-                    if (r < nrows) {  // rows past nrows have no probabilities this tile
-                        const float4 p4 = *reinterpret_cast<const float4 *>(pg + r * kKeys + k4);
-                        float2 o = acc[r];
-                        o = ffma2(make_float2(p4.x, p4.x), vv[0], o);
-                        o = ffma2(make_float2(p4.y, p4.y), vv[1], o);
-                        o = ffma2(make_float2(p4.z, p4.z), vv[2], o);
-                        o = ffma2(make_float2(p4.w, p4.w), vv[3], o);
-                        acc[r] = o;
+                if (lane == 0) {
+                    // keys past the cache's capacity read as zeros; keys past the range or the
+                    // sequence length are masked in the softmax
+                    const int key0 = u.k_begin + kDecTile * t;
+                    uint8_t *kd = smem + L::kRingOff + s * 2 * L::kTileBytes;
+                    mbar_arrive_expect_tx(&kv_full[s], 2 * L::kTileBytes);
+                    for (int b = 0; b < L::kBoxes; ++b) {
+                        tma_load_3d(kd + b * L::kBoxBytes, &tmk, b * 64, key0, u.kvh, &kv_full[s]);
+                        tma_load_3d(kd + L::kTileBytes + b * L::kBoxBytes, &tmv, b * 64, key0,
+                                    u.kvh, &kv_full[s]);
                     }
                 }
+                ++n;
+                // the first K/V tile goes ahead of Q: its slot frees before the Q tile does
+                if (!q_done) {
+                    ok = load_q();
+                    q_done = true;
+                }
+            }
+            if (ok && !q_done) ok = load_q();  // a unit without keys still takes its Q turn
+            if (!ok) break;
+            // next unit: a CTA of this grid that has not started, cancelled for us
+            int next = -1;
+            if (more) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(sched, 16);
+                    clc_try_cancel(sched_answer, sched);
+                }
+                ++nreq;
+                if (!mbar_wait_warp(sched, (nreq - 1) & 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                next = clc_cancelled_x(sched_answer);
+                if (next >= static_cast<int>(gridDim.x)) next = -1;
+                more = next >= 0;
+            }
+            // publish it (or the end) in slot (k + 1) & 1, once unit k - 1 has released it
+            const int e2 = (k + 1) & 1;
+            if (k >= 1 && !mbar_wait_warp(&unit_empty[e2], ((k + 1) / 2 - 1) & 1, p.ctl,
+                                          abort_flag)) {
+                ok = false;
+                break;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                unit_slot[e2] = next;
+                mbar_arrive(&unit_full[e2]);
+            }
+            if (next < 0) break;
+            unit = next;
+        }
+        if (!ok || *abort_flag) {
+            // let every copy and request still in flight land before shared memory goes away
+            if (lane == 0) {
+                if (nq > 0) drain_wait(q_full, (nq - 1) & 1, p.ctl);
+                if (nreq > 0) drain_wait(sched, (nreq - 1) & 1, p.ctl);
+                for (int l = n > L::kStages ? n - L::kStages : 0; l < n; ++l)
+                    drain_wait(&kv_full[l % L::kStages], (l / L::kStages) & 1, p.ctl);
             }
         }
-    }
-    if (*abort_flag) {
-        // let the copies still in flight land before shared memory is reused or released
-        if (tid == 0)
-            for (int u = t; u < min(ntiles, t + kStages - 1); ++u)
-                drain_wait(&full[u % kStages], (u / kStages) & 1, p.ctl);
-        __syncthreads();
-        return;
-    }
-
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        const SDesc dq = sdesc_make(smem_u32(smem + L::kQOff), 16, 1024);       // Q: K-major
+        const SDesc dk0 = sdesc_make(smem_u32(smem + L::kRingOff), 16, 1024);   // K: K-major
+        const SDesc dv0 = sdesc_make(smem_u32(smem + L::kRingOff + L::kTileBytes), L::kBoxBytes,
+                                     1024);                                      // V: MN-major
+        int n = 0;  // K/V tile pairs used (all units): tile n's S goes into buffer n % 2
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int e = k & 1;
+            if (!mbar_wait_warp(&unit_full[e], (k >> 1) & 1, p.ctl, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const int unit = unit_slot[e];
+            if (unit < 0) break;
+            const DecUnit u = dec_unit(p, unit);
+            if (!mbar_wait_warp(q_full, k & 1, p.ctl, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            auto issue_s = [&](int t) -> bool {  // S of the unit's tile t (ring tile n + t)
+                const int g = n + t;
+                const int s = g % L::kStages;
+                if (!mbar_wait_warp(&kv_full[s], (g / L::kStages) & 1, p.ctl, abort_flag))
+                    return false;
+                tc_fence_after();
+                const SDesc b = sdesc_add(dk0, s * 2 * L::kTileBytes);
+                if constexpr (D == 128)
+                    mma_ss_chain_k128(tmem + (g & 1) * 128, dq, b, kIdescS, 0u);
+                else
+                    mma_ss_chain_k64(tmem + (g & 1) * 128, dq, b, kIdescS, 0u);
+                umma_commit_el(&s_full[g & 1]);
+                if (t == u.ntiles - 1) umma_commit_el(q_empty);  // the unit's last S: Q is free
+                return true;
+            };
+            if (u.ntiles == 0) {
+                umma_commit_el(q_empty);
+            } else if (!issue_s(0)) {
+                ok = false;
+                break;
+            }
+            for (int t = 0; ok && t < u.ntiles; ++t) {
+                if (t + 1 < u.ntiles && !issue_s(t + 1)) {  // S_{t+1} ahead of PV_t
+                    ok = false;
+                    break;
+                }
+                const int g = n + t;
+                if (!mbar_wait_warp(&p_full[g & 1], (g >> 1) & 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int s = g % L::kStages;
+                mma_ts_chain_k128(tmem + 256, tmem + (g & 1) * 128,
+                                  sdesc_add(dv0, s * 2 * L::kTileBytes), kIdescPV, t > 0 ? 1u : 0u);
+                umma_commit_el(pv_done);
+                umma_commit_el(&kv_empty[s]);
+            }
+            if (!ok) break;
+            n += u.ntiles;
+            if (u.ntiles > 0) umma_commit_el(o_final);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&unit_empty[e]);
+        }
+        // every MMA issued above completes before the CTA releases TMEM and smem
+        umma_commit_el(drain);
+        drain_wait(drain, 0, p.ctl);
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        using T = elem_t<BF16>;
+        const int quad = warp & 3;  // a warp may touch TMEM lanes [32*(warp%4), +32)
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tO = tmem + lane_base + 256;
+        const float sl2 = p.scale_log2;
+        int g = 0;     // K/V tiles consumed (all units)
+        int nfin = 0;  // units with keys (o_final phases)
+        for (int k = 0;; ++k) {
+            const int e = k & 1;
+            if (!mbar_wait_warp(&unit_full[e], (k >> 1) & 1, p.ctl, abort_flag)) break;
+            const int unit = unit_slot[e];
+            if (unit < 0) break;
+            const DecUnit u = dec_unit(p, unit);
+            const bool busy = quad * 32 < u.nrows;  // this quarter holds real rows
+            // the last key this row may see: its own position when causal (new rows end-aligned
+            // with the cache), the sequence's last key otherwise
+            const int gr = u.r0 + row;
+            const int last = p.causal ? u.len - p.Nq + gr % p.Nq : u.len - 1;
+            float m = -INFINITY;  // running (reference) max of the scaled scores, log2 units
+            float l = 0.f;        // running sum of exp2(score - m)
+            bool ok = true;
+            for (int t = 0; t < u.ntiles; ++t, ++g) {
+                if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, p.ctl, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (busy) {
+                    const uint32_t tS = tmem + lane_base + (g & 1) * 128;
+                    uint32_t r[128];
+                    tmem_ld32(tS + 0, r + 0);
+                    tmem_ld32(tS + 32, r + 32);
+                    tmem_ld32(tS + 64, r + 64);
+                    tmem_ld32(tS + 96, r + 96);
+                    tmem_wait_ld();
+                    const int kv0 = u.k_begin + kDecTile * t;
+                    const int lim = min(u.k_end - 1, last);  // keys above lim are masked
+                    if (kv0 + kDecTile - 1 > lim) {
 #pragma unroll
-    for (int i = 0; i < kRowsA2; ++i) {
-        const int r = warp + 4 * i;
-        if (r < nrows && lane == 0) {
-            m_s[r] = m_run[i];
-            l_s[r] = l_run[i];
+                        for (int c = 0; c < 128; ++c)
+                            if (kv0 + c > lim) r[c] = __float_as_uint(-INFINITY);
+                    }
+                    const float m_tile = row_max128(r) * sl2;
+                    const float m_new = fmaxf(m, m_tile);
+                    const bool old_finite = m != -INFINITY;
+                    const bool grow = m_new > m + 8.0f;
+                    float alpha = 1.f;
+                    if (grow) {
+                        if (old_finite) alpha = ex2(m - m_new);
+                        l *= alpha;
+                        m = m_new;
+                    }
+                    const bool rescale = grow && old_finite;
+                    const float mu = m == -INFINITY ? 0.f : m;  // a row with nothing unmasked yet
+                    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                     make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    const float2 sc2 = make_float2(sl2, sl2), mu2 = make_float2(-mu, -mu);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const float2 x = ffma2(make_float2(__uint_as_float(r[64 * h + 2 * c]),
+                                                               __uint_as_float(r[64 * h + 2 * c + 1])),
+                                                   sc2, mu2);
+                            const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+                            acc[c & 3] = fadd2(acc[c & 3], ev);
+                            pk[c] = pack2<BF16>(ev.x, ev.y);
+                        }
+                        tmem_st32(tS + 32 * h, pk);
+                    }
+                    const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+                    const float2 a = fadd2(a01, a23);
+                    l += a.x + a.y;
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        // O holds the products up to PV_{t-1}, which S_t did not wait for: let
+                        // it complete before O is rescaled (the next PV waits for p_full)
+                        if (!mbar_wait_warp(pv_done, (g - 1) & 1, p.ctl, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + cc * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int x = 0; x < 32; ++x)
+                                o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                            tmem_st32(tO + cc * 32, o);
+                        }
+                    }
+                }
+                mbar_arrive_warp_after_st(&p_full[g & 1]);
+            }
+            if (!ok) break;
+            if (u.ntiles > 0) {
+                if (!mbar_wait_warp(o_final, nfin & 1, p.ctl, abort_flag)) break;
+                ++nfin;
+                tc_fence_after();
+            }
+            // rows of this unit: O = O~ / l and LSE, or the range's partial (m, l, O~); the
+            // tensor-memory loads are warp-wide, the stores only for real rows
+            if (busy) {
+                const bool real = row < u.nrows;
+                const long grow = u.grow0 + row;
+                const long prow = static_cast<long>(u.split) * total_rows + grow;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    if (u.ntiles > 0) {
+                        tmem_ld32(tO + cc * 32, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) o[x] = 0u;
+                    }
+                    if (!real) continue;
+                    if (p.splits == 1) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.o) +
+                                                               grow * D + cc * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                w[x] = pack2<BF16>(__uint_as_float(o[8 * q4 + 2 * x]) * inv,
+                                                   __uint_as_float(o[8 * q4 + 2 * x + 1]) * inv);
+                            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + cc * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                                  __uint_as_float(o[4 * q4 + 2]),
+                                                  __uint_as_float(o[4 * q4 + 3]));
+                    }
+                }
+                if (real) {
+                    if (p.splits == 1)
+                        p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    else
+                        reinterpret_cast<float2 *>(p.part_ml)[prow] = make_float2(m, l);
+                }
+            }
+            // O has been read out (the next unit's first PV waits for this warp's next p_full
+            // arrival); the unit slot is no longer needed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&unit_empty[e]);
         }
     }
-    __syncthreads();  // every thread is past its last read of the K/V ring
-    // merge of the key groups: group g's partial output of row r at red[(g * RPC + r) * D]
-    float *red = reinterpret_cast<float *>(smem);
-#pragma unroll
-    for (int r = 0; r < RPC; ++r)
-        if (r < nrows) reinterpret_cast<float2 *>(red + (rs * RPC + r) * D)[cp] = acc[r];
+
+    tc_fence_before();
     __syncthreads();
-    const long total_rows = static_cast<long>(p.B) * p.H * p.Nq;
-#pragma unroll
-    for (int j = 0; j < kRowsB; ++j) {
-        const int r = rs + kRB * j;
-        if (r >= nrows) continue;
-        float2 o = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int g = 0; g < kRB; ++g) {  // fixed order: deterministic
-            const float2 x = reinterpret_cast<const float2 *>(red + (g * RPC + r) * D)[cp];
-            o.x += x.x;
-            o.y += x.y;
-        }
-        const long grow = grow0 + r;
-        const float m = m_s[r], l = l_s[r];
-        if (p.splits == 1) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            reinterpret_cast<uint32_t *>(reinterpret_cast<T *>(p.o) + grow * D)[cp] =
-                pack2<BF16>(o.x * inv, o.y * inv);
-            if (cp == 0)
-                p.lse[grow] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        } else {
-            const long prow = static_cast<long>(split) * total_rows + grow;
-            reinterpret_cast<float2 *>(p.part_o + prow * D)[cp] = o;
-            if (cp == 0) reinterpret_cast<float2 *>(p.part_ml)[prow] = make_float2(m, l);
-        }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
@@ -415,27 +569,16 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     if (lane == 0) p.lse[row] = l > 0.f ? (M + __log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D, bool BF16, int RPC>
-cudaError_t launch_decode_rpc(const DecodeMaps &m, const DecodeParams &p, cudaStream_t stream) {
-    using L = DecLayout<D, RPC>;
-    auto kern = fa_decode_kernel<D, BF16, RPC>;
+template <int D, bool BF16>
+cudaError_t launch_decode_t(const DecodeMaps &m, const DecodeParams &p, cudaStream_t stream) {
+    using L = DecLayout<D>;
+    auto kern = fa_decode_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kAlloc);
     if (e != cudaSuccess) return e;
     const long grid = static_cast<long>(p.B) * p.Hkv * p.splits * p.row_groups;
-    kern<<<static_cast<unsigned>(grid), kThreads, L::kAlloc, stream>>>(m.k, m.v, p);
-    return cudaGetLastError();
-}
-
-template <int D, bool BF16>
-cudaError_t launch_decode_t(const DecodeMaps &m, const DecodeParams &p, cudaStream_t stream) {
-    const int rpc = p.rows >= 16 ? 16 : p.rows;  // rows per CTA: the row group size
-    cudaError_t e;
-    if (rpc <= 1) e = launch_decode_rpc<D, BF16, 1>(m, p, stream);
-    else if (rpc <= 2) e = launch_decode_rpc<D, BF16, 2>(m, p, stream);
-    else if (rpc <= 4) e = launch_decode_rpc<D, BF16, 4>(m, p, stream);
-    else if (rpc <= 8) e = launch_decode_rpc<D, BF16, 8>(m, p, stream);
-    else e = launch_decode_rpc<D, BF16, 16>(m, p, stream);
+    kern<<<static_cast<unsigned>(grid), L::kThreads, L::kAlloc, stream>>>(m.q, m.k, m.v, p);
+    e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;
     // programmatic stream serialization: the merge's CTAs (small: 128 threads, 2 KB) are
     // scheduled beside the range kernel's last CTAs instead of after its completion

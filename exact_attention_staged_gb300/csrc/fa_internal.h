@@ -145,15 +145,16 @@ struct DecodeParams {
     float *part_ml;           //             [splits][B*H*Nq][2] running max (log2) and sum
     int B, H, Hkv, Nq, Nk;
     int rows;                 // (H / H_kv) * Nq: query rows that share one K/V head
-    int row_groups;           // ceil(rows / 16): CTAs per K/V head and key range
-    int splits, chunk;        // key ranges [s * chunk, (s + 1) * chunk), chunk a multiple of 32
+    int row_groups;           // ceil(rows / 128): work units per K/V head and key range
+    int splits, chunk;        // key ranges [s * chunk, (s + 1) * chunk), chunk a multiple of 128
     float scale_log2;         // scale * log2(e)
     int causal;               // new rows end-aligned with the cache
     Ctl ctl;
 };
 
 struct DecodeMaps {
-    CUtensorMap k, v;         // [B*H_kv, Nk, d] cache, boxes 64 elements x 16 keys
+    CUtensorMap q;            // [B*H*Nq, d] query rows (one z slice), boxes 64 elements x 128 rows
+    CUtensorMap k, v;         // [B*H_kv, Nk, d] cache, boxes 64 elements x 128 keys
 };
 
 struct Maps {

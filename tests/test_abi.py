@@ -150,15 +150,17 @@ def test_gqa_workspace_and_validation(lib):
 
 def test_decode_workspace_and_validation(lib):
     p = ctypes.c_void_p(16)
-    # 16 sequences x 8 K/V heads at 8k: 128 CTAs per key range; about 28 CTAs per SM of a
-    # 152-SM GPU would take 4256 / 128 = 33 ranges, capped at 8192 / 256 = 32 (of 256 keys)
+    # 16 sequences x 8 K/V heads at 8k: 128 units per key range; about eight units per SM of a
+    # 152-SM GPU take ceil(1216 / 128) = 10 ranges, of ceil(8192 / 10) = 820 keys rounded up to
+    # 896 (seven 128-key tiles): 10 ranges
     rows = 16 * 32 * 1
-    assert api.decode_workspace_bytes(16, 32, 8, 1, 8192, 128) == 32 * rows * (128 + 2) * 4
-    # 2 sequences x 2 K/V heads at 64k: 4256 / 4 = 1064 ranges of 64 keys would be too short;
-    # 65536 / 256 = 256 ranges of 256 keys
-    assert api.decode_workspace_bytes(2, 8, 2, 1, 65536, 64) == 256 * 16 * (64 + 2) * 4
-    # 256 keys or fewer: a single range, no scratch
+    assert api.decode_workspace_bytes(16, 32, 8, 1, 8192, 128) == 10 * rows * (128 + 2) * 4
+    # 2 sequences x 2 K/V heads at 64k: 304 ranges would be shorter than 512 keys;
+    # 65536 / 512 = 128 ranges
+    assert api.decode_workspace_bytes(2, 8, 2, 1, 65536, 64) == 128 * 16 * (64 + 2) * 4
+    # 512 keys or fewer: a single range, no scratch
     assert api.decode_workspace_bytes(2, 4, 4, 1, 200, 64) == 0
+    assert api.decode_workspace_bytes(2, 4, 4, 1, 512, 64) == 0
     assert lib.fa_decode_workspace_bytes(1, 6, 4, 1, 100, 64) == 0  # 4 does not divide 6
 
     def dec(q=p, kv_len=None, B=1, H=4, Hkv=2, Nq=1, Nk=128, d=64, ws=None, wsb=0):
