@@ -415,17 +415,13 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             uint32_t keep = 0;  // dropout: bit c set = query 32g + c of tile i keeps this key row
             if constexpr (DROP) {
                 // lane l draws the bits of query 32g + l for the warp's 32 key rows (one
-                // generator block) before the scores are ready; the ballots hand lane r the bits
-                // of its own key row
+                // generator block) before the scores are ready; a bit transpose hands lane r the
+                // bits of its own key row
                 const uint32_t mine = philox_keep_bits(
                     static_cast<uint64_t>(kt) * 4 + quad,
                     static_cast<uint64_t>(i * kTile + kGroupCols * g + lane),
                     static_cast<uint64_t>(hq), p.drop);
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const uint32_t col = __ballot_sync(0xffffffffu, (mine >> r) & 1u);
-                    if (lane == r) keep = col;
-                }
+                keep = transpose32_bits(mine, lane);
             }
             // S^T of this tile: buffer n % 2 at d = 64, the only one otherwise
             const uint32_t tS = tS0 + ((L::kDbl && (n & 1)) ? 384u : 0u);
@@ -862,11 +858,10 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
             if (!tile_live(p, mrow, qt, j, j)) continue;
             const int b = n & 1;
             const uint32_t tS = tmem + lane_base + 128 * b + kGroupCols * g;
-            uint32_t keep = 0xffffffffu;  // dropout: bit e set = key 128 j + 32 g + e is kept
+            uint32_t keep[8];  // dropout: keep flag of key 128 j + 32 g + e in byte e % 4 of word e / 4
             if constexpr (DROP)
-                keep = philox_keep_bits(static_cast<uint64_t>(j) * 4 + g,
-                                        static_cast<uint64_t>(q_row), static_cast<uint64_t>(bh),
-                                        p.drop);
+                philox_keep_flags(static_cast<uint64_t>(j) * 4 + g, static_cast<uint64_t>(q_row),
+                                  static_cast<uint64_t>(bh), p.drop, keep);
             if (!mbar_wait_warp(&s_full[b], (n >> 1) & 1, p.ctl, abort_flag)) {
                 ok = false;
                 break;
@@ -908,9 +903,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 if constexpr (DROP) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        bv[e] = __float_as_uint(((keep >> e) & 1u)
-                                                    ? __uint_as_float(bv[e]) * p.drop.keep_scale
-                                                    : 0.f);
+                        bv[e] = __float_as_uint(__uint_as_float(bv[e]) * p.drop.keep_scale) &
+                                keep_elem_mask(keep[e >> 2], e & 3);
                 }
                 uint32_t w[16];
                 const float2 d2 = make_float2(drow, drow);

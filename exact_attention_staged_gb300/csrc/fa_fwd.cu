@@ -490,11 +490,13 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int j = 0; j < u.jend; ++j) {
                 if (!fwd_live(p, mr, qt, j)) continue;
-                uint32_t keep[4];  // dropout: keep bits of keys 32w .. 32w + 31 of this tile, drawn
-                if constexpr (DROP) {  // while the tensor core still works on S
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        keep[w] = philox_keep_bits(4u * j + w, q_row, u.bh, p.drop);
+                // dropout: keep flags of the 64 keys of one half of the tile (keys 32w .. 32w + 31
+                // in keep[w % 2]); the first half's are drawn while the tensor core still works
+                // on S, the second half's once the first half's P is stored
+                uint32_t keep[2][8];
+                if constexpr (DROP) {
+                    philox_keep_flags(4u * j, q_row, u.bh, p.drop, keep[0]);
+                    philox_keep_flags(4u * j + 1, q_row, u.bh, p.drop, keep[1]);
                 }
                 if (!mbar_wait_warp(&s_full[t], scnt & 1, p.ctl, abort_flag)) {
                     ok = false;
@@ -535,6 +537,12 @@ __global__ void __launch_bounds__(384, 1)
                 const float2 sc2 = make_float2(sl2, sl2), mu2 = make_float2(-mu, -mu);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
+                    if constexpr (DROP) {
+                        if (h == 1) {
+                            philox_keep_flags(4u * j + 2, q_row, u.bh, p.drop, keep[0]);
+                            philox_keep_flags(4u * j + 3, q_row, u.bh, p.drop, keep[1]);
+                        }
+                    }
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -544,7 +552,9 @@ __global__ void __launch_bounds__(384, 1)
                         const float2 ev = make_float2(ex2(x.x), ex2(x.y));
                         acc[c & 3] = fadd2(acc[c & 3], ev);
                         pk[c] = pack2<BF16>(ev.x, ev.y);
-                        if constexpr (DROP) pk[c] = keep_halves(pk[c], keep[2 * h + (c >> 4)], c & 15);
+                        if constexpr (DROP)  // keys 64h + 2c, + 1: bytes 2(c % 2), + 1 of word (c % 16) / 2
+                                             // of chunk c / 16 of this half
+                            pk[c] &= keep_pair_mask(keep[c >> 4][(c & 15) >> 1], 2 * (c & 1));
                     }
                     tmem_st32(tS + 32 * h, pk);
                 }

@@ -62,6 +62,66 @@ __device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, ui
     return bits;
 }
 
+// The same 32 decisions as keep flags: the top bit of byte b of word i is set when key
+// 32 kb + 4 i + b is kept (the other bits carry no meaning).  A byte x is kept when x >= t, i.e.
+// when the 8-bit sum x + (256 - t) carries out; the carries of all four bytes of a word come from
+// one add of the low seven bits of each byte (no carry crosses a byte) and a bitwise majority of
+// the two top bits and that sum's top bit.  Three instructions per four decisions.
+__device__ __forceinline__ void philox_keep_flags(uint64_t kb, uint64_t q, uint64_t bh,
+                                                  const DropSpec &ds, uint32_t flags[8]) {
+    uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
+             a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
+    uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
+    uint32_t k0 = static_cast<uint32_t>(ds.seed), k1 = static_cast<uint32_t>(ds.seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        philox4x32_round(a0, a1, a2, a3, k0, k1);
+        philox4x32_round(b0, b1, b2, b3, k0, k1);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
+    const uint32_t c4 = (256u - (ds.t4 & 0xFFu)) * 0x01010101u;  // 256 - t in every byte (t >= 1)
+    const uint32_t c4lo = c4 & 0x7F7F7F7Fu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t s7 = (w[i] & 0x7F7F7F7Fu) + c4lo;
+        uint32_t f;
+        asm("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(f) : "r"(w[i]), "r"(c4), "r"(s7));  // majority
+        flags[i] = f;
+    }
+}
+
+// Mask keeping the 16-bit halves of a packed pair whose keep flags are bytes `byte` and
+// `byte` + 1 of `flags` (top bits): prmt copies each selected byte's top bit over its byte.
+__device__ __forceinline__ uint32_t keep_pair_mask(uint32_t flags, int byte) {
+    const uint32_t sel = (8u | byte) * 0x11u | ((8u | (byte + 1)) * 0x11u) << 8;
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(flags), "r"(sel));
+    return m;
+}
+// All-ones when the keep flag in byte `byte` of `flags` is set, else zero.
+__device__ __forceinline__ uint32_t keep_elem_mask(uint32_t flags, int byte) {
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(flags), "r"((8u | byte) * 0x1111u));
+    return m;
+}
+
+// Transpose of the 32 x 32 bit matrix whose row l is `x` of lane l: returns, to lane r, the word
+// whose bit c is bit r of lane c's `x`.  Five butterfly stages; at stage j, lanes l and l ^ j swap
+// the j-bit blocks in which they differ (the lane with bit j clear gives its high blocks and takes
+// its partner's low ones, shifted up).  Every lane of the warp calls it.
+__device__ __forceinline__ uint32_t transpose32_bits(uint32_t x, int lane) {
+    const uint32_t m[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int j = 16 >> s;
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) == 0 ? (x & m[s]) | ((y & m[s]) << j) : (x & ~m[s]) | ((y >> j) & m[s]);
+    }
+    return x;
+}
+
 // Zero the 16-bit halves of `w` (elements 2c and 2c + 1 of a row) whose keep bit is clear.
 __device__ __forceinline__ uint32_t keep_halves(uint32_t w, uint32_t bits, int c) {
     const uint32_t lo = (bits >> (2 * c)) & 1u, hi = (bits >> (2 * c + 1)) & 1u;
