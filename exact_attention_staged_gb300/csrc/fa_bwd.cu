@@ -423,6 +423,9 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                     static_cast<uint64_t>(hq), p.drop);
                 keep = transpose32_bits(mine, lane);
             }
+            // keep bits 4w .. 4w + 3 as keep flags (to the top bits of bytes 0 .. 3): the
+            // product's other terms land on distinct lower bits, so no carry reaches a top bit
+            auto kf = [&](int w) { return ((keep >> (4 * w)) & 0xFu) * 0x10204080u; };
             // S^T of this tile: buffer n % 2 at d = 64, the only one otherwise
             const uint32_t tS = tS0 + ((L::kDbl && (n & 1)) ? 384u : 0u);
             uint64_t *const sbar = &s_full[L::kDbl ? (n & 1) : 0];
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
             if constexpr (DROP) {  // dV sees the dropped probabilities, dS all of them
                 uint32_t pkd[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) pkd[c] = keep_halves(pk[c], keep, c);
+                for (int c = 0; c < 16; ++c) pkd[c] = pk[c] & keep_pair_mask(kf(c >> 1), 2 * (c & 1));
                 tmem_st16(tS, pkd);
             } else {
                 tmem_st16(tS, pk);
@@ -490,9 +493,8 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 if constexpr (DROP) {  // dP of a dropped score is 0, of a kept one dP / (1 - p)
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        r[c] = __float_as_uint(((keep >> c) & 1u)
-                                                   ? __uint_as_float(r[c]) * p.drop.keep_scale
-                                                   : 0.f);
+                        r[c] = __float_as_uint(__uint_as_float(r[c]) * p.drop.keep_scale) &
+                               static_cast<uint32_t>(static_cast<int32_t>(keep << (31 - c)) >> 31);
                 }
                 uint32_t w[16];
 #pragma unroll
