@@ -340,7 +340,7 @@ int run_dq(const void *q, const void *k, const void *v, const void *dout, const 
 }
 
 int run_preprocess(const void *o, const void *dout, float *delta, int B, int H, int N, int d,
-                   int dtype, void *stream) {
+                   int dtype, void *stream, float mul = 1.f) {
     int rc = check_shape(B, H, N, d, dtype, 1.f);
     if (rc != FA_OK) return rc;
     rc = check_ptrs({o, dout, delta});
@@ -349,7 +349,8 @@ int run_preprocess(const void *o, const void *dout, float *delta, int B, int H, 
     rc = device_setup(&dev, &status);
     if (rc != FA_OK) return rc;
     cudaError_t e = fa::launch_bwd_preprocess(o, dout, delta, static_cast<long>(B) * H * N, d,
-                                              dtype == FA_BF16, static_cast<cudaStream_t>(stream));
+                                              dtype == FA_BF16, mul,
+                                              static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -362,7 +363,12 @@ int run_bwd(const void *q, const void *k, const void *v, const void *o, const vo
             const float *lse, void *dq, void *dk, void *dv, float *delta, const DkvSplit &sp,
             float *part, int B, int H, int Hkv, int N, int d, int dtype, float scale, int causal,
             const uint8_t *mask, const fa::DropSpec &drop, void *stream) {
-    int rc = run_preprocess(o, dout, delta, B, H, N, d, dtype, stream);
+    // with dropout the passes take D / s (s = 256 / (256 - t) the keep scale): dS = s P o (Z o dP
+    // - D / s), so a kept dP needs no multiply and dK, dQ take the factor s at the end
+    const float dmul =
+        drop.t4 != 0 ? static_cast<float>((256.0 - static_cast<double>(drop.t4 & 0xFFu)) / 256.0)
+                     : 1.f;
+    int rc = run_preprocess(o, dout, delta, B, H, N, d, dtype, stream, dmul);
     if (rc != FA_OK) return rc;
     if (sp.splits == 1) {
         rc = run_dq(q, k, v, dout, lse, delta, dq, B, H, Hkv, N, d, dtype, scale, causal, mask,

@@ -86,7 +86,7 @@ constexpr int kComputeWarps = kComputeThreads / 32;
 // ================================================================================ preprocess
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, const void *dout,
-                                                                float *delta, long rows) {
+                                                                float *delta, long rows, float mul) {
     constexpr int kLanes = D / 8;  // 8 elements (16 bytes) per lane
     // queued right after the forward with programmatic stream serialization: O is complete and
     // visible only past this point
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const void *o, c
     }
 #pragma unroll
     for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && part == 0) delta[row] = acc;
+    if (row < rows && part == 0) delta[row] = acc * mul;
 }
 
 // ================================================================================ dK / dV
@@ -493,8 +493,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 if constexpr (DROP) {  // dP of a dropped score is 0, of a kept one dP / (1 - p)
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                        r[c] = __float_as_uint(__uint_as_float(r[c]) * p.drop.keep_scale) &
-                               static_cast<uint32_t>(static_cast<int32_t>(keep << (31 - c)) >> 31);
+                        r[c] &= static_cast<uint32_t>(static_cast<int32_t>(keep << (31 - c)) >> 31);
                 }
                 uint32_t w[16];
 #pragma unroll
@@ -527,7 +526,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
         // warp reaches the named barrier, whether or not its waits succeeded.
         const int half = g & 1;
         const uint32_t tacc = tmem + lane_base + 256 + (g < 2 ? 0 : D) + half * (D / 2);
-        const float mul = g < 2 ? (DROP ? p.drop.keep_scale : 1.f) : p.scale;
+        const float mul = (DROP ? p.drop.keep_scale : 1.f) * (g < 2 ? 1.f : p.scale);
         if (p.part == nullptr) {
             if (ok) {
                 uint8_t *stage = smem + L::kSlotOff + (g < 2 ? 0 : 1) * L::kTileBytes;
@@ -905,8 +904,7 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                 if constexpr (DROP) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        bv[e] = __float_as_uint(__uint_as_float(bv[e]) * p.drop.keep_scale) &
-                                keep_elem_mask(keep[e >> 2], e & 3);
+                        bv[e] &= keep_elem_mask(keep[e >> 2], e & 3);
                 }
                 uint32_t w[16];
                 const float2 d2 = make_float2(drow, drow);
@@ -944,7 +942,8 @@ __global__ void __launch_bounds__(96 + kComputeThreads, 1)
                     for (int e = 0; e < 16; ++e) a[e] = 0u;
                 }
                 const int col = g * (D / 4) + 16 * cc;
-                st_box_row<BF16, 16>(stage + (col >> 6) * L::kBoxBytes, row, col & 63, a, p.scale);
+                st_box_row<BF16, 16>(stage + (col >> 6) * L::kBoxBytes, row, col & 63, a,
+                                     DROP ? p.scale * p.drop.keep_scale : p.scale);
             }
             fence_proxy_async_smem();
         }
@@ -1005,7 +1004,7 @@ __global__ void __launch_bounds__(256) fa_bwd_group_reduce_kernel(const float *p
 // just before (the usual order, forward then backward), this small kernel's CTAs are scheduled
 // beside its last CTAs instead of after its completion; it waits for that grid before reading.
 template <int D, bool BF16>
-cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long rows,
+cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long rows, float mul,
                          cudaStream_t stream) {
     const long threads = rows * (D / 8);
     const long blocks = (threads + 255) / 256;
@@ -1018,7 +1017,7 @@ cudaError_t launch_pre_t(const void *o, const void *dout, float *delta, long row
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fa_bwd_preprocess_kernel<D, BF16>, o, dout, delta, rows);
+    return cudaLaunchKernelEx(&cfg, fa_bwd_preprocess_kernel<D, BF16>, o, dout, delta, rows, mul);
 }
 
 // after_dq: the launch directly follows the dQ pass of the same backward call on `stream`; it is
@@ -1061,11 +1060,11 @@ cudaError_t launch_dq_t(const Maps &m, const BwdParams &p, cudaStream_t stream) 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const void *o, const void *dout, float *delta, long rows,
-                                  int d, bool bf16, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_pre_t<64, true>(o, dout, delta, rows, stream)
-                             : launch_pre_t<64, false>(o, dout, delta, rows, stream);
-    return bf16 ? launch_pre_t<128, true>(o, dout, delta, rows, stream)
-                : launch_pre_t<128, false>(o, dout, delta, rows, stream);
+                                  int d, bool bf16, float mul, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_pre_t<64, true>(o, dout, delta, rows, mul, stream)
+                             : launch_pre_t<64, false>(o, dout, delta, rows, mul, stream);
+    return bf16 ? launch_pre_t<128, true>(o, dout, delta, rows, mul, stream)
+                : launch_pre_t<128, false>(o, dout, delta, rows, mul, stream);
 }
 
 cudaError_t launch_bwd_group_reduce(const float *part, void *dk, void *dv, int splits,

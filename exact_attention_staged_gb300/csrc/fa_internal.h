@@ -164,8 +164,9 @@ struct Maps {
 
 cudaError_t launch_fwd(const Maps &maps, const FwdParams &p, int d, bool bf16,
                        cudaStream_t stream);
+// delta[row] = mul * rowsum(dout o o)
 cudaError_t launch_bwd_preprocess(const void *o, const void *dout, float *delta, long rows,
-                                  int d, bool bf16, cudaStream_t stream);
+                                  int d, bool bf16, float mul, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const Maps &maps, const BwdParams &p, int d, bool bf16,
                             bool after_dq, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const Maps &maps, const BwdParams &p, int d, bool bf16,
