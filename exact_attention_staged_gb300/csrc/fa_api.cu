@@ -135,7 +135,7 @@ int tiles_of(int N) { return (N + fa::kTile - 1) / fa::kTile; }
 // Dropout decisions: drop probability p -> byte threshold t = nearest integer to 256 p (ties to
 // even), valid for 0 <= t <= 255; t = 0 turns dropout off.  The offset is a 32-bit counter word
 // of the generator.
-constexpr fa::DropSpec kNoDrop = {0u, 1.f, 0ull, 0ull};
+constexpr fa::DropSpec kNoDrop = {0u, 1.f, 0ull, 0ull, {}};
 int make_drop(float p, unsigned long long seed, unsigned long long offset, fa::DropSpec *out) {
     if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID;
     if (offset > 0xFFFFFFFFull) return FA_ERR_INVALID;  // a 32-bit counter word
@@ -145,6 +145,7 @@ int make_drop(float p, unsigned long long seed, unsigned long long offset, fa::D
     out->keep_scale = static_cast<float>(256.0 / (256.0 - static_cast<double>(t)));
     out->seed = seed;
     out->offset = offset;
+    fa::philox_round_keys(*out);
     return FA_OK;
 }
 

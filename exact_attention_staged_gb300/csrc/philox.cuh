@@ -14,12 +14,30 @@
 
 namespace fa {
 
+constexpr int kPhiloxRounds = 10;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;  // key increments
+
 struct DropSpec {
     uint32_t t4;        // threshold t in each byte (t * 0x01010101); 0: no dropout
     float keep_scale;   // 256 / (256 - t)
     uint64_t seed;      // key
     uint64_t offset;    // counter word 3 (below 2^32)
+    // the key of every round, (k0, k1) = (seed mod 2^32 + r W0, seed div 2^32 + r W1) mod 2^32:
+    // the same for every counter, so they are worked out once on the host and read from the
+    // kernel's parameter block
+    uint32_t round_key[kPhiloxRounds][2];
 };
+
+// Fill in the round keys of ds.seed.
+__host__ __device__ inline void philox_round_keys(DropSpec &ds) {
+    uint32_t k0 = static_cast<uint32_t>(ds.seed), k1 = static_cast<uint32_t>(ds.seed >> 32);
+    for (int r = 0; r < kPhiloxRounds; ++r) {
+        ds.round_key[r][0] = k0;
+        ds.round_key[r][1] = k1;
+        k0 += kPhiloxW0;
+        k1 += kPhiloxW1;
+    }
+}
 
 // One Philox4x32 round on counter (c0, c1, c2, c3) under round key (k0, k1).
 __device__ __forceinline__ void philox4x32_round(uint32_t &c0, uint32_t &c1, uint32_t &c2,
@@ -42,13 +60,10 @@ __device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, ui
     uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
              a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
     uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
-    uint32_t k0 = static_cast<uint32_t>(ds.seed), k1 = static_cast<uint32_t>(ds.seed >> 32);
 #pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        philox4x32_round(a0, a1, a2, a3, k0, k1);
-        philox4x32_round(b0, b1, b2, b3, k0, k1);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+    for (int r = 0; r < kPhiloxRounds; ++r) {
+        philox4x32_round(a0, a1, a2, a3, ds.round_key[r][0], ds.round_key[r][1]);
+        philox4x32_round(b0, b1, b2, b3, ds.round_key[r][0], ds.round_key[r][1]);
     }
     const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
     uint32_t bits = 0;
@@ -72,13 +87,10 @@ __device__ __forceinline__ void philox_keep_flags(uint64_t kb, uint64_t q, uint6
     uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
              a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
     uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
-    uint32_t k0 = static_cast<uint32_t>(ds.seed), k1 = static_cast<uint32_t>(ds.seed >> 32);
 #pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        philox4x32_round(a0, a1, a2, a3, k0, k1);
-        philox4x32_round(b0, b1, b2, b3, k0, k1);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+    for (int r = 0; r < kPhiloxRounds; ++r) {
+        philox4x32_round(a0, a1, a2, a3, ds.round_key[r][0], ds.round_key[r][1]);
+        philox4x32_round(b0, b1, b2, b3, ds.round_key[r][0], ds.round_key[r][1]);
     }
     const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
     const uint32_t c4 = (256u - (ds.t4 & 0xFFu)) * 0x01010101u;  // 256 - t in every byte (t >= 1)
