@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(64 + kComputeThreads, 1)
                 // lane l draws the bits of query 32g + l for the warp's 32 key rows (one
                 // generator block) before the scores are ready; a bit transpose hands lane r the
                 // bits of its own key row
-                const uint32_t mine = philox_keep_bits(
+                const uint32_t mine = philox_keep_bits<false>(
                     static_cast<uint64_t>(kt) * 4 + quad,
                     static_cast<uint64_t>(i * kTile + kGroupCols * g + lane),
                     static_cast<uint64_t>(hq), p.drop);

@@ -55,24 +55,40 @@ __device__ __forceinline__ void philox4x32_round(uint32_t &c0, uint32_t &c1, uin
 // Keep bits of the 32 scores k = 32 kb .. 32 kb + 31 of query row q: bit j set = key 32 kb + j
 // is kept.  The two generator blocks (counters 2 kb and 2 kb + 1) run interleaved, sharing the
 // key schedule.
+// kHostKeys: read each round's key from ds.round_key (fewer instructions), else advance the key
+// in registers (fewer registers held: the dK/dV compute warps run at 96 per thread).
+template <bool kHostKeys = true>
 __device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, uint64_t bh,
                                                      const DropSpec &ds) {
     uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
              a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
     uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
+    uint32_t k0 = static_cast<uint32_t>(ds.seed), k1 = static_cast<uint32_t>(ds.seed >> 32);
 #pragma unroll
     for (int r = 0; r < kPhiloxRounds; ++r) {
-        philox4x32_round(a0, a1, a2, a3, ds.round_key[r][0], ds.round_key[r][1]);
-        philox4x32_round(b0, b1, b2, b3, ds.round_key[r][0], ds.round_key[r][1]);
+        if constexpr (kHostKeys) {
+            k0 = ds.round_key[r][0];
+            k1 = ds.round_key[r][1];
+        }
+        philox4x32_round(a0, a1, a2, a3, k0, k1);
+        philox4x32_round(b0, b1, b2, b3, k0, k1);
+        if constexpr (!kHostKeys) {
+            k0 += kPhiloxW0;
+            k1 += kPhiloxW1;
+        }
     }
     const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
+    const uint32_t c4 = (256u - (ds.t4 & 0xFFu)) * 0x01010101u;  // as in philox_keep_flags
+    const uint32_t c4lo = c4 & 0x7F7F7F7Fu;
     uint32_t bits = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // bytes 4i .. 4i + 3 of the 32 (keys 32 kb + 4i ..)
-        // 0xFF in every byte at or above the threshold; one bit per byte gathered by a product
-        // whose partial terms land on distinct bit positions (no carries)
-        const uint32_t ge = __vcmpgeu4(w[i], ds.t4) & 0x01010101u;
-        bits |= ((ge * 0x01020408u) >> 24) << (4 * i);
+        const uint32_t s7 = (w[i] & 0x7F7F7F7Fu) + c4lo;
+        uint32_t f;
+        asm("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(f) : "r"(w[i]), "r"(c4), "r"(s7));
+        // the four top bits to bits 28..31 by a product whose other terms land on distinct
+        // lower bits (no carries)
+        bits |= (((f & 0x80808080u) * 0x00204081u) >> 28) << (4 * i);
     }
     return bits;
 }
