@@ -2,7 +2,9 @@
 oracle (``oracle.dropout``), which draws the same Philox4x32-10 decisions independently.
 
 Tolerances as in test_parity_gpu: dropout only zeroes probabilities and scales the rest by
-256 / (256 - t), so the rounding behaviour of O and the gradients is that of the plain path.
+256 / (256 - t), so the rounding behaviour of O and the gradients is that of the plain path,
+on values that factor larger: the relative bars are unchanged and O's max-abs bar is scaled by
+256 / (256 - t) (at p = 0.9 O is about ten times the plain output, and so is its rounding).
 """
 import math
 
@@ -33,7 +35,17 @@ CASES = [  # B, H, N, d, causal, p
     (2, 2, 513, 64, True, 0.5),
     (1, 3, 384, 128, False, 0.1),
     (1, 1, 17, 64, True, 0.3),
+    # thresholds above 128 (256 - t below 128: the other branch of the kernels' byte compare),
+    # the largest one, and the smallest nonzero one
+    (1, 2, 256, 64, False, 0.75),
+    (1, 1, 200, 128, True, 0.9),
+    (1, 2, 130, 128, False, 0.99),
+    (1, 2, 130, 64, True, 1 / 256),
 ]
+
+
+def keep_scale(p):
+    return 256.0 / (256.0 - odrop.threshold(p))
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,p", CASES)
@@ -44,7 +56,7 @@ def test_dropout_small(cuda_lib, B, H, N, d, causal, p):
     ref = odrop.attention_dropout(t["q"], t["k"], t["v"], scale, p, 1234 + N, 7, causal,
                                   dout=t["do"])
     what = f"B={B} H={H} N={N} d={d} causal={causal} p={p}"
-    check_fwd(o, lse, ref, what)
+    check_fwd(o, lse, ref, what, o_scale=keep_scale(p))
     check_bwd(grads, ref, what)
 
 
