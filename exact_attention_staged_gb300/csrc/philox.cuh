@@ -52,14 +52,14 @@ __device__ __forceinline__ void philox4x32_round(uint32_t &c0, uint32_t &c1, uin
     c3 = lo0;
 }
 
-// Keep bits of the 32 scores k = 32 kb .. 32 kb + 31 of query row q: bit j set = key 32 kb + j
-// is kept.  The two generator blocks (counters 2 kb and 2 kb + 1) run interleaved, sharing the
-// key schedule.
-// kHostKeys: read each round's key from ds.round_key (fewer instructions), else advance the key
-// in registers (fewer registers held: the dK/dV compute warps run at 96 per thread).
-template <bool kHostKeys = true>
-__device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, uint64_t bh,
-                                                     const DropSpec &ds) {
+// The eight output words of the two generator blocks with counters (2 kb, q, bh, offset) and
+// (2 kb + 1, q, bh, offset), run interleaved: their bytes decide the 32 scores
+// k = 32 kb .. 32 kb + 31 of query row q (byte k mod 32 of the 32).  kHostKeys: read each round's
+// key from ds.round_key (fewer instructions), else advance the key in registers (fewer registers
+// held: the dK/dV compute warps run at 96 per thread).
+template <bool kHostKeys>
+__device__ __forceinline__ void philox_pair(uint64_t kb, uint64_t q, uint64_t bh,
+                                            const DropSpec &ds, uint32_t w[8]) {
     uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
              a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
     uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
@@ -77,47 +77,52 @@ __device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, ui
             k1 += kPhiloxW1;
         }
     }
-    const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
-    const uint32_t c4 = (256u - (ds.t4 & 0xFFu)) * 0x01010101u;  // as in philox_keep_flags
-    const uint32_t c4lo = c4 & 0x7F7F7F7Fu;
+    w[0] = a0; w[1] = a1; w[2] = a2; w[3] = a3;
+    w[4] = b0; w[5] = b1; w[6] = b2; w[7] = b3;
+}
+
+// Keep flags of the four bytes of `w`: the top bit of byte b is set when that byte is kept (the
+// other bits carry no meaning).  A byte x is kept when x >= t, i.e. when the 8-bit sum
+// x + (256 - t) carries out; the carries of all four bytes come from one add of the low seven
+// bits of each byte (no carry crosses a byte) and a bitwise majority of the two top bits and
+// that sum's top bit.  c4 = (256 - t) * 0x01010101 (t >= 1).  Three instructions.
+__device__ __forceinline__ uint32_t keep_flags4(uint32_t w, uint32_t c4) {
+    const uint32_t s7 = (w & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
+    uint32_t f;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(f) : "r"(w), "r"(c4), "r"(s7));  // majority
+    return f;
+}
+__device__ __forceinline__ uint32_t keep_c4(const DropSpec &ds) {
+    return (256u - (ds.t4 & 0xFFu)) * 0x01010101u;
+}
+
+// Keep bits of the 32 scores k = 32 kb .. 32 kb + 31 of query row q: bit j set = key 32 kb + j
+// is kept.
+template <bool kHostKeys = true>
+__device__ __forceinline__ uint32_t philox_keep_bits(uint64_t kb, uint64_t q, uint64_t bh,
+                                                     const DropSpec &ds) {
+    uint32_t w[8];
+    philox_pair<kHostKeys>(kb, q, bh, ds, w);
+    const uint32_t c4 = keep_c4(ds);
     uint32_t bits = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // bytes 4i .. 4i + 3 of the 32 (keys 32 kb + 4i ..)
-        const uint32_t s7 = (w[i] & 0x7F7F7F7Fu) + c4lo;
-        uint32_t f;
-        asm("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(f) : "r"(w[i]), "r"(c4), "r"(s7));
         // the four top bits to bits 28..31 by a product whose other terms land on distinct
         // lower bits (no carries)
-        bits |= (((f & 0x80808080u) * 0x00204081u) >> 28) << (4 * i);
+        bits |= (((keep_flags4(w[i], c4) & 0x80808080u) * 0x00204081u) >> 28) << (4 * i);
     }
     return bits;
 }
 
-// The same 32 decisions as keep flags: the top bit of byte b of word i is set when key
-// 32 kb + 4 i + b is kept (the other bits carry no meaning).  A byte x is kept when x >= t, i.e.
-// when the 8-bit sum x + (256 - t) carries out; the carries of all four bytes of a word come from
-// one add of the low seven bits of each byte (no carry crosses a byte) and a bitwise majority of
-// the two top bits and that sum's top bit.  Three instructions per four decisions.
+// The same 32 decisions as keep flags: word i holds those of keys 32 kb + 4 i .. + 3, one per
+// byte (keep_flags4).
 __device__ __forceinline__ void philox_keep_flags(uint64_t kb, uint64_t q, uint64_t bh,
                                                   const DropSpec &ds, uint32_t flags[8]) {
-    uint32_t a0 = static_cast<uint32_t>(2 * kb), a1 = static_cast<uint32_t>(q),
-             a2 = static_cast<uint32_t>(bh), a3 = static_cast<uint32_t>(ds.offset);
-    uint32_t b0 = a0 + 1, b1 = a1, b2 = a2, b3 = a3;
+    uint32_t w[8];
+    philox_pair<true>(kb, q, bh, ds, w);
+    const uint32_t c4 = keep_c4(ds);
 #pragma unroll
-    for (int r = 0; r < kPhiloxRounds; ++r) {
-        philox4x32_round(a0, a1, a2, a3, ds.round_key[r][0], ds.round_key[r][1]);
-        philox4x32_round(b0, b1, b2, b3, ds.round_key[r][0], ds.round_key[r][1]);
-    }
-    const uint32_t w[8] = {a0, a1, a2, a3, b0, b1, b2, b3};
-    const uint32_t c4 = (256u - (ds.t4 & 0xFFu)) * 0x01010101u;  // 256 - t in every byte (t >= 1)
-    const uint32_t c4lo = c4 & 0x7F7F7F7Fu;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t s7 = (w[i] & 0x7F7F7F7Fu) + c4lo;
-        uint32_t f;
-        asm("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(f) : "r"(w[i]), "r"(c4), "r"(s7));  // majority
-        flags[i] = f;
-    }
+    for (int i = 0; i < 8; ++i) flags[i] = keep_flags4(w[i], c4);
 }
 
 // Mask keeping the 16-bit halves of a packed pair whose keep flags are bytes `byte` and
@@ -148,12 +153,6 @@ __device__ __forceinline__ uint32_t transpose32_bits(uint32_t x, int lane) {
         x = (lane & j) == 0 ? (x & m[s]) | ((y & m[s]) << j) : (x & ~m[s]) | ((y >> j) & m[s]);
     }
     return x;
-}
-
-// Zero the 16-bit halves of `w` (elements 2c and 2c + 1 of a row) whose keep bit is clear.
-__device__ __forceinline__ uint32_t keep_halves(uint32_t w, uint32_t bits, int c) {
-    const uint32_t lo = (bits >> (2 * c)) & 1u, hi = (bits >> (2 * c + 1)) & 1u;
-    return w & ((lo * 0xFFFFu) | (hi * 0xFFFF0000u));
 }
 
 }  // namespace fa
