@@ -46,7 +46,7 @@ METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak"
 DEFAULT_WORKLOAD = "gpt_causal_d128_n8k"
 L2_BYTES = 129e6  # GB300 L2 (129 MB)
 _CSRC = "exact_attention_staged_gb300/csrc/"
-_SHARED = (_CSRC + "sm100.cuh", _CSRC + "fa_internal.h")
+_SHARED = (_CSRC + "sm100.cuh", _CSRC + "fa_internal.h", _CSRC + "philox.cuh")
 # Files whose content decides each kernel's code: a stored ncu traffic figure is used only
 # while their combined hash (comments left out) still matches the one recorded with it.
 KERNEL_SOURCES = {
@@ -56,6 +56,9 @@ KERNEL_SOURCES = {
     "fa_bwd_preprocess_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
     "fa_decode_kernel": (_CSRC + "fa_decode.cu",) + _SHARED,
     "fa_decode_combine_kernel": (_CSRC + "fa_decode.cu",) + _SHARED,
+    "fa_bwd_group_reduce_kernel": (_CSRC + "fa_bwd.cu",) + _SHARED,
+    "fa_fwd_fp8_kernel": (_CSRC + "fa_fwd_fp8.cu",) + _SHARED,
+    "fa_fp8_transpose_v_kernel": (_CSRC + "fa_fwd_fp8.cu",) + _SHARED,
 }
 
 
@@ -540,7 +543,8 @@ def run_gpu(args, w):
     peak = peaks["bf16_tflops"]
     roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": ncu_traffic(dominant, w.name),
+                "traffic": (ncu_traffic(dominant, w.name) if dominant in KERNEL_SOURCES
+                            else backward_call_traffic(w.name)),
                 "peak_kind": f"bf16 dense burst ({peaks['source']})",
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "timing": timing}
@@ -699,6 +703,25 @@ def decode_work(w, t):
     nbytes = 2 * w.h_kv * cache_rows * w.d * esz + 2 * w.B * w.H * w.Nq * w.d * esz + \
         4 * w.B * w.H * w.Nq
     return fl, nbytes
+
+
+def calls_traffic(workload, kernels):
+    """DRAM bytes of a sequence of kernels (one launch each) from the committed ncu summary,
+    or None if any of them has no record or changed since."""
+    per = [ncu_traffic(k, workload) for k in kernels]
+    return None if not per or any(x is None for x in per) else sum(per)
+
+
+def backward_call_traffic(workload):
+    """DRAM bytes of one backward call (every recorded kernel of the workload but the
+    forward), or None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            kernels = [k for k in json.load(f).get(workload, {}) if k != "fa_fwd_kernel"]
+    except (OSError, ValueError):
+        return None
+    return calls_traffic(workload, kernels)
 
 
 def decode_traffic(workload, nws):
@@ -899,7 +922,9 @@ def run_fp8_gpu(args, w):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": "fa_fp8_transpose_v_kernel + fa_fwd_fp8_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": calls_traffic(w.name, ["fa_fp8_transpose_v_kernel",
+                                                       "fa_fwd_fp8_kernel"]),
                      "peak_kind": f"e4m3 dense = 2 x bf16 dense burst ({peaks['source']})"},
         "cpu_baseline": None,
         "e2e": {"value": world * fl * e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
