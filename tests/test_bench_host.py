@@ -123,6 +123,22 @@ def test_stored_traffic_is_used_only_while_the_kernel_sources_match(monkeypatch)
     assert bench.decode_traffic("decode_gqa_d128_kv8k", 1) is None
 
 
+def test_call_traffic_is_the_sum_of_its_kernels_records(monkeypatch):
+    # a backward call (the dominant unit of the grouped-query and dropout lines) counts every
+    # recorded kernel of its workload but the forward; any kernel without a valid record voids it
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        stored = json.load(f)
+    for workload in ("dropout_causal_d128_n8k", "gqa_causal_d128_n8k"):
+        kernels = [k for k in stored.get(workload, {}) if k != "fa_fwd_kernel"]
+        parts = [bench.ncu_traffic(k, workload) for k in kernels]
+        if kernels and all(x is not None for x in parts):
+            assert bench.backward_call_traffic(workload) == sum(parts)
+    assert bench.calls_traffic("no_such_workload", ["fa_fwd_kernel"]) is None
+    assert bench.calls_traffic("gpt_causal_d128_n8k", []) is None
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "fa_bwd_dq_kernel", ("bench.py",))
+    assert bench.backward_call_traffic("dropout_causal_d128_n8k") is None
+
+
 def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     src = 'int f(int x) {  // doubles\n  /* "quoted" */ return 2 * x; }\nconst char *s = "a // b";\n'
     (tmp_path / "a.cu").write_text(src)
