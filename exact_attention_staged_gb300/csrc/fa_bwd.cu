@@ -7,7 +7,7 @@
 // The atomic dQ update of Algorithm 2 is replaced by a second, query-stationary pass, so every
 // output element is written once by one CTA: the result is deterministic.
 //
-//   preprocess   D = rowsum(dO o O), one group of lanes per row, fp32.
+//   preprocess   D = rowsum(dO o O) (times a given factor), one group of lanes per row, fp32.
 //   dK/dV        CTA = one 128-row key tile j of one head (K_j, V_j stay in smem).  For every
 //                live query tile i (causal: i >= j; block mask: M[i][j] != 0):
 //                  S^T = K_j Q_i^T, dP^T = V_j dO_i^T     (SS MMAs into TMEM)
@@ -22,6 +22,10 @@
 // In both, four groups of four warps split every 128 x 128 score tile into four 32-wide column
 // quarters (one TMEM lane quadrant per warp of a group), and the MMA warps run one tile ahead so
 // the groups' exponentials overlap the tensor core (see each kernel's comment for its order).
+// With dropout (keep scale s = 256 / (256 - t), keep decisions Z regenerated as in the forward):
+// dV takes the dropped P (Z o P) and the factor s at the end; dP is masked to Z o dP, and since
+// dS = P o (s Z o dP - D) = s P o (Z o dP - D / s), the preprocess writes D / s and dK, dQ take
+// the factor s at the end with the softmax scale.
 #include "fa_internal.h"
 
 #include <cmath>
